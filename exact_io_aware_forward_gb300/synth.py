@@ -1,0 +1,107 @@
+"""Seeded synthetic inputs for exact attention.
+
+This module only draws random tensors; it holds none of the attention
+arithmetic.  Both the CUDA path (tests, bench) and the float64 oracle take
+their inputs from here, so the two sides always see the same values.
+
+Two recipes:
+
+* ``attention_inputs`` -- the workload shapes used for the GPU path:
+  Q, K, V and dO i.i.d. N(0, 1) in float32, drawn in that order from
+  ``torch.Generator('cpu').manual_seed(seed)``, then rounded to fp16/bf16.
+  With ``k_row_scale=True`` every K row (per batch, head and position) is
+  multiplied by a factor drawn from U(0.5, 3) *before* the rounding, which
+  widens the range of the scores and exercises the online rescale.  The
+  factor tensor is drawn after V and before dO.
+* ``page_inputs`` -- the float64 workload of the tutorial page
+  "FlashAttention 为什么不需要存下注意力矩阵" (jefxiong.cn), section 04:
+  ``numpy.random.default_rng(seed).normal(size=(N, D))`` drawn three times
+  for Q, K, V of one head.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One attention problem: shapes, dtype, mask and seed."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str
+    causal: bool
+    seed: int
+    k_row_scale: bool = False
+    backward: bool = True
+
+    @property
+    def heads(self) -> int:
+        return self.B * self.H
+
+    def fwd_flops(self) -> float:
+        """4*B*H*N^2*d, halved under the causal mask."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+
+# The five workloads the path is specified on (shapes, dtypes, masks).
+C1 = Workload("C1 fwd non-causal N=256 d=64 fp16", 1, 1, 256, 64, "fp16", False, 0, backward=False)
+C2 = Workload("C2 fwd+bwd causal N=1024 d=64 fp16", 4, 16, 1024, 64, "fp16", True, 1)
+C3N = Workload("C3 fwd+bwd non-causal N=4096 d=64 bf16 K-row-scaled", 2, 16, 4096, 64, "bf16", False, 2, True)
+C3C = Workload("C3 fwd+bwd causal N=4096 d=64 bf16 K-row-scaled", 2, 16, 4096, 64, "bf16", True, 2, True)
+C4 = Workload("C4 fwd+bwd causal N=8192 d=128 bf16", 2, 32, 8192, 128, "bf16", True, 3)
+C5 = Workload("C5 fwd+bwd causal N=32768 d=128 bf16", 1, 8, 32768, 128, "bf16", True, 4)
+WORKLOADS = {"C1": C1, "C2": C2, "C3N": C3N, "C3C": C3C, "C4": C4, "C5": C5}
+
+
+def attention_inputs(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int = 0,
+                     k_row_scale: bool = False, with_do: bool = True):
+    """Return (q, k, v, do) CPU tensors of shape [B, H, N, d] in ``dtype``.
+
+    ``do`` is None when ``with_do`` is False.  The draws are made in float32
+    and rounded once to the 16-bit type (round to nearest even).
+    """
+    if dtype not in DTYPES:
+        raise ValueError(f"dtype must be one of {sorted(DTYPES)}, got {dtype!r}")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    if k_row_scale:
+        factor = torch.rand((B, H, N, 1), generator=g, dtype=torch.float32) * 2.5 + 0.5
+        k = k * factor
+    do = torch.randn(shape, generator=g, dtype=torch.float32) if with_do else None
+    t = DTYPES[dtype]
+    return (q.to(t), k.to(t), v.to(t), None if do is None else do.to(t))
+
+
+def workload_inputs(w: Workload, with_do: bool | None = None):
+    """Inputs of a named workload (see ``WORKLOADS``)."""
+    if with_do is None:
+        with_do = w.backward
+    return attention_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.k_row_scale, with_do)
+
+
+def page_inputs(N: int, D: int, seed: int):
+    """float64 Q, K, V of one head, drawn like the tutorial page's demos."""
+    rng = np.random.default_rng(seed)
+    q = rng.normal(size=(N, D))
+    k = rng.normal(size=(N, D))
+    v = rng.normal(size=(N, D))
+    return q, k, v
+
+
+def as_float64(*tensors):
+    """Exact upcast of 16-bit tensors to float64 numpy arrays (None passes)."""
+    return tuple(None if t is None else t.to(torch.float64).numpy() for t in tensors)

@@ -1,0 +1,139 @@
+"""Plain float64 softmax attention with S and P materialised.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+Definitions followed
+--------------------
+* Forward: P1 section 2.1 (Attention = softmax(QK^T/sqrt(d_k)) V) and P3
+  section 3.1 (safe softmax: subtract the row max, exponentiate, divide by
+  the row sum).  The scale ``s`` is a parameter; the pages use 1/sqrt(d).
+* Causal mask: P3 section 3.2 (masked scores are set to -inf so they add
+  nothing to m, l or O); key j is visible to query i iff j <= i (top-left
+  alignment, square problem).
+* LSE: P3 section 3.2, natural log: LSE_i = m_i + log(l_i) with m_i the row
+  max of the *scaled* scores.
+* Backward: P3 section 3.3 -- with G = dO and A = G V^T,
+  dS = P * (A - rowsum(A * P)), dQ = s * dS K, dK = s * dS^T Q, dV = P^T G.
+  The row sum is taken over A * P exactly as written there, not through the
+  rowsum(dO * O) shortcut the CUDA path uses.
+
+Arrays are numpy float64.  Batched entry points take [B, H, N, d] arrays and
+loop over heads; the ``*_head`` functions take one head [N, d].
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# building blocks (kept separate so that tests can plant mistakes in them)
+# --------------------------------------------------------------------------
+def _scores(q, k, scale, causal, rows=None):
+    """S = s * Q K^T for the query rows ``rows`` (all rows if None).
+
+    Causal: entries with key index > query index become -inf (P3 section 3.2).
+    """
+    if rows is None:
+        rows = np.arange(q.shape[0])
+    rows = np.asarray(rows)
+    s = scale * (q[rows] @ k.T)
+    if causal:
+        keys = np.arange(k.shape[0])
+        s = np.where(keys[None, :] > rows[:, None], -np.inf, s)
+    return s
+
+
+def _softmax_rows(s):
+    """Safe softmax of every row (P3 section 3.1).
+
+    Returns (P, m, l) with m the row max and l = sum exp(s - m).
+    """
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    l = e.sum(axis=1)
+    return e / l[:, None], m, l
+
+
+def _softmax_backward(p, a):
+    """dS = P * (A - rowsum(A * P)) (P3 section 3.3)."""
+    return p * (a - (a * p).sum(axis=1, keepdims=True))
+
+
+# --------------------------------------------------------------------------
+# one head
+# --------------------------------------------------------------------------
+def forward_head(q, k, v, scale, causal=False, rows=None):
+    """O and LSE of one head ([N, d] inputs) for the query rows ``rows``."""
+    s = _scores(q, k, scale, causal, rows)
+    p, m, l = _softmax_rows(s)
+    return p @ v, m + np.log(l)
+
+
+def probabilities_head(q, k, scale, causal=False, rows=None):
+    """The full softmax matrix P of one head (for invariant checks)."""
+    p, _, _ = _softmax_rows(_scores(q, k, scale, causal, rows))
+    return p
+
+
+def backward_head(q, k, v, do, scale, causal=False):
+    """(dQ, dK, dV) of one head, everything materialised (P3 section 3.3)."""
+    p, _, _ = _softmax_rows(_scores(q, k, scale, causal))
+    a = do @ v.T
+    ds = _softmax_backward(p, a)
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    dv = p.T @ do
+    return dq, dk, dv
+
+
+def backward_head_sampled(q, k, v, do, scale, causal, rows, cols, stripe=2048):
+    """dQ at query rows ``rows`` and dK, dV at key rows ``cols`` of one head.
+
+    The same definition as ``backward_head``; S, P and A are built in stripes
+    of ``stripe`` query rows so that a long head fits in host memory.  dK and
+    dV at a key j need column j of dS for every query, so every stripe is
+    visited; dQ at a query i needs only row i.
+    """
+    n = q.shape[0]
+    rows = np.asarray(rows)
+    cols = np.asarray(cols)
+    dk = np.zeros((len(cols), q.shape[1]))
+    dv = np.zeros((len(cols), v.shape[1]))
+    for r0 in range(0, n, stripe):
+        r = np.arange(r0, min(n, r0 + stripe))
+        p, _, _ = _softmax_rows(_scores(q, k, scale, causal, r))
+        a = do[r] @ v.T
+        ds = _softmax_backward(p, a)
+        dk += scale * (ds[:, cols].T @ q[r])
+        dv += p[:, cols].T @ do[r]
+    p, _, _ = _softmax_rows(_scores(q, k, scale, causal, rows))
+    ds = _softmax_backward(p, do[rows] @ v.T)
+    dq = scale * (ds @ k)
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# batched [B, H, N, d]
+# --------------------------------------------------------------------------
+def forward(q, k, v, scale, causal=False):
+    """O [B,H,N,d] and LSE [B,H,N] of every head."""
+    B, H, N, d = q.shape
+    o = np.empty((B, H, N, v.shape[-1]))
+    lse = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            o[b, h], lse[b, h] = forward_head(q[b, h], k[b, h], v[b, h], scale, causal)
+    return o, lse
+
+
+def backward(q, k, v, do, scale, causal=False):
+    """dQ, dK, dV [B,H,N,d] of every head."""
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    B, H = q.shape[:2]
+    for b in range(B):
+        for h in range(H):
+            dq[b, h], dk[b, h], dv[b, h] = backward_head(
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+    return dq, dk, dv
