@@ -1,0 +1,10 @@
+"""Exact IO-aware softmax attention for GB300 (sm_103a).
+
+The compute lives in ``libfa_gb300.so`` (hand-written tcgen05/TMA kernels,
+C ABI in ``include/fa_gb300.h``); ``api`` is its thin Python binding.
+Importing this package does not load the library; the first call does, and
+fails loudly if it has not been built.
+"""
+from .api import (FAError, backward, fa_backward, fa_backward_dkdv, fa_backward_dq_convert,  # noqa: F401
+                  fa_backward_preprocess, fa_backward_workspace_size, fa_device_status, fa_forward,
+                  forward)

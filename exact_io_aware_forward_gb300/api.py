@@ -1,0 +1,145 @@
+"""Python binding of the C ABI in ``include/fa_gb300.h``.
+
+Argument marshalling only: the functions named like the C entry points take
+torch CUDA tensors, check dtype/shape/contiguity, and pass raw device
+pointers plus the current CUDA stream to the library.  Every step of the
+computation runs in the library's kernels.  ``forward`` and ``backward`` are
+conveniences that also allocate the outputs (and the backward workspace)
+with torch.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from ._lib import lib, status_string
+
+FA_FP16, FA_BF16 = 0, 1
+_DTYPE_CODE = {torch.float16: FA_FP16, torch.bfloat16: FA_BF16}
+
+
+class FAError(RuntimeError):
+    """A non-zero fa_status returned by the library."""
+
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {code}: {status_string(code)}")
+        self.code = code
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise FAError(fn, code)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes_stream(stream)
+
+
+def ctypes_stream(stream) -> int:
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _bhnd(name, t, like=None, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [B, H, N, d]")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if like is not None and tuple(t.shape) != tuple(like):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(like)}")
+    return t.data_ptr()
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    if q.dtype not in _DTYPE_CODE:
+        raise TypeError("q must be float16 or bfloat16")
+    return tuple(q.shape)
+
+
+def _scale(scale, d):
+    return float(1.0 / math.sqrt(d) if scale is None else scale)
+
+
+# ---------------------------------------------------------------- C entry points
+def fa_forward(q, k, v, o, lse, causal=False, scale=None, stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt),
+            _bhnd("o", o, q.shape, dt), _bhnd("lse", lse, (B, H, N), torch.float32)]
+    _check("fa_forward", lib().fa_forward(*args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)),
+                                          _scale(scale, d), _stream(stream)))
+
+
+def fa_backward_workspace_size(B, H, N, d) -> int:
+    return int(lib().fa_backward_workspace_size(B, H, N, d))
+
+
+def fa_backward(q, k, v, o, do, lse, dq, dk, dv, workspace, causal=False, scale=None, stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("o", o, q.shape, dt),
+            _bhnd("do", do, q.shape, dt), _bhnd("lse", lse, (B, H, N), torch.float32),
+            _bhnd("dq", dq, q.shape, dt), _bhnd("dk", dk, q.shape, dt), _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward", lib().fa_backward(*args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)),
+                                            _scale(scale, d), workspace.data_ptr(), workspace.numel(),
+                                            _stream(stream)))
+
+
+def fa_backward_preprocess(o, do, delta, dq_accum, stream=None) -> None:
+    B, H, N, d = _shape(o)
+    dt = o.dtype
+    args = [_bhnd("o", o), _bhnd("do", do, o.shape, dt), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dq_accum", dq_accum, o.shape, torch.float32)]
+    _check("fa_backward_preprocess",
+           lib().fa_backward_preprocess(*args, B, H, N, d, _DTYPE_CODE[dt], _stream(stream)))
+
+
+def fa_backward_dkdv(q, k, v, do, lse, delta, dq_accum, dk, dv, causal=False, scale=None, stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dq_accum", dq_accum, q.shape, torch.float32), _bhnd("dk", dk, q.shape, dt),
+            _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_dkdv", lib().fa_backward_dkdv(*args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)),
+                                                      _scale(scale, d), _stream(stream)))
+
+
+def fa_backward_dq_convert(dq_accum, dq, scale=None, stream=None) -> None:
+    B, H, N, d = _shape(dq)
+    args = [_bhnd("dq_accum", dq_accum, dq.shape, torch.float32), _bhnd("dq", dq)]
+    _check("fa_backward_dq_convert", lib().fa_backward_dq_convert(*args, B, H, N, d, _DTYPE_CODE[dq.dtype],
+                                                                  _scale(scale, d), _stream(stream)))
+
+
+def fa_device_status(stream=None) -> None:
+    """Synchronise ``stream``; raise FAError if a kernel latched a timeout."""
+    _check("fa_device_status", lib().fa_device_status(_stream(stream)))
+
+
+# ---------------------------------------------------------------- conveniences
+def forward(q, k, v, causal=False, scale=None, stream=None):
+    """Return (O, LSE) for [B, H, N, d] q, k, v."""
+    B, H, N, d = _shape(q)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    fa_forward(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, causal=False, scale=None, stream=None, workspace=None):
+    """Return (dQ, dK, dV)."""
+    B, H, N, d = _shape(q)
+    if workspace is None:
+        workspace = torch.empty(fa_backward_workspace_size(B, H, N, d), device=q.device, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_backward(q, k, v, o, do, lse, dq, dk, dv, workspace, causal, scale, stream)
+    return dq, dk, dv

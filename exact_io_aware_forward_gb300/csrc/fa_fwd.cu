@@ -1,0 +1,449 @@
+// Forward pass of exact attention on sm_103a.
+//
+// Algorithm: the online-softmax recurrence of "FlashAttention 为什么不需要存下
+// 注意力矩阵" (jefxiong.cn), section 3.2 -- per query row a reference max m, a
+// denominator l and an unnormalised accumulator O; a new key tile with
+// larger scores rescales l and O by exp(m_old - m_new); the output is O / l
+// and the saved statistic is LSE = m + ln l.  The loop order is queries
+// outer, keys inner (the order the same page's section 05 attributes to
+// FlashAttention-2), so O never leaves the chip until the end.
+//
+// Mapping onto one CTA (384 threads, one CTA per SM):
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j through a ring of
+//               shared-memory slots (128-byte swizzle, 64-column slabs).
+//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//               S_t = Q_t K_j^T (fp32 in TMEM) and O_t += P_t V_j with P_t
+//               read from TMEM.
+//   warps 4-7   softmax for query tile 0 (rows q0 .. q0+127),
+//   warps 8-11  softmax for query tile 1 (rows q0+128 .. q0+255): each
+//               thread owns one row (one TMEM lane), reads the 128 scores
+//               of its row, updates m and l in the log2 domain with ex2,
+//               writes P as packed 16-bit pairs over the S columns, and
+//               rescales its O row in TMEM when needed.  The two tiles
+//               ping-pong: while one softmax runs, the tensor core works
+//               on the other tile.  At the end the same warps normalise O
+//               and write their rows of O and LSE.
+//
+// Rescaling is lazy: the reference max of a row only moves when the new
+// row max exceeds it by more than 8 (log2 units, i.e. a factor 256).  O and
+// l always share one reference, so O / l and m + ln l are unchanged (the
+// invariant of section 3.2 holds for any common reference; the max only
+// prevents overflow, and 2^8 keeps every P below 256).  Two sums are kept:
+// l over P in fp32 (for LSE) and l_mma over P as rounded to 16 bit for the
+// PV product (for normalising O).
+//
+// Causal: key tiles entirely above the diagonal are never loaded or
+// multiplied (section 4.5's whole-block skip); the diagonal tile and the
+// ragged tail (keys >= N) are masked elementwise to -inf.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;  // query rows per tile (tcgen05 M)
+  static constexpr int BN = 128;  // keys per tile (tcgen05 N of S)
+  static constexpr int QT = 2;    // query tiles per CTA
+  static constexpr int SLAB = 128 * 64 * 2;  // 128 rows x 64 columns x 16 bit
+  static constexpr int SLABS = D / 64;
+  static constexpr int TILE = SLABS * SLAB;  // one 128 x D tile
+  static constexpr int NS = D == 128 ? 5 : 8;  // K/V ring slots
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = QT * TILE;
+  static constexpr int OFF_BAR = OFF_RING + NS * TILE;
+  // q_full, ring_full[NS], ring_empty[NS], s_full[2], p_full[2], o_full, drain
+  static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t TMEM_COLS = 512;  // S0 | S1 | O0 | O1
+  static constexpr uint32_t COL_S = 0;
+  static constexpr uint32_t COL_O = 256;
+};
+
+__device__ __forceinline__ void unpack2(uint32_t v, bool bf16, float& lo, float& hi) {
+  if (bf16) {
+    lo = __uint_as_float(v << 16);
+    hi = __uint_as_float(v & 0xffff0000u);
+  } else {
+    __half2 h = *reinterpret_cast<__half2*>(&v);
+    float2 f = __half22float2(h);
+    lo = f.x;
+    hi = f.y;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Bounded wait whose result is the same on every lane of the warp, so that
+// warp-collective tcgen05 instructions after it are never split.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned int* status) {
+  const bool ok = mbar_wait(bar, parity, abort, status, kStatusTimeout);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait used only on the abort path: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return;
+  }
+}
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(384, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o,
+                  float* __restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
+                  unsigned int* status) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sRing = smem + C::OFF_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* ring_full = bars + 1;
+  uint64_t* ring_empty = ring_full + C::NS;
+  uint64_t* s_full = ring_empty + C::NS;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = p_full + 2;
+  uint64_t* drain = o_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Heaviest work first: the last query blocks see the most keys under the mask.
+  const int bh = blockIdx.x % BH;
+  const int qb = n_qblocks - 1 - blockIdx.x / BH;
+  const int q0 = qb * (C::QT * C::BM);
+  const int n_kv = (N + C::BN - 1) / C::BN;
+  const int n0 = CAUSAL ? min(n_kv, q0 / C::BN + 1) : n_kv;  // key tiles seen by query tile 0
+  const int n1 = CAUSAL ? min(n_kv, q0 / C::BN + 2) : n_kv;  // ... and by query tile 1
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto kslot = [](int j) { return (2 * j) % C::NS; };
+  auto kpar = [](int j) { return (uint32_t)(((2 * j) / C::NS) & 1); };
+  auto vslot = [](int j) { return (2 * j + 1) % C::NS; };
+  auto vpar = [](int j) { return (uint32_t)(((2 * j + 1) / C::NS) & 1); };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;  // K/V tiles whose copy has been started
+      mbar_arrive_expect_tx(q_full, C::QT * C::TILE);
+      for (int t = 0; t < C::QT; ++t)
+        for (int s = 0; s < C::SLABS; ++s)
+          tma_load_3d(sQ + t * C::TILE + s * C::SLAB, &tm_q, q_full, s * 64, q0 + t * C::BM, bh);
+      for (int u = 0; u < 2 * n1; ++u) {
+        const int slot = u % C::NS;
+        const uint32_t use = (uint32_t)(u / C::NS);
+        if (!mbar_wait(&ring_empty[slot], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
+        mbar_arrive_expect_tx(&ring_full[slot], C::TILE);
+        const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
+        for (int s = 0; s < C::SLABS; ++s)
+          tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, (u >> 1) * C::BN, bh);
+        issued = u + 1;
+      }
+      if (*abort_flag) {  // let every copy in flight land before the CTA exits
+        drain_wait(q_full, 0);
+        for (int u = issued - C::NS < 0 ? 0 : issued - C::NS; u < issued; ++u)
+          drain_wait(&ring_full[u % C::NS], (uint32_t)((u / C::NS) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(128, C::BN, BF16, false, false);
+      constexpr uint32_t kIdPV = idesc_f16(128, D, BF16, false, true);
+      const uint32_t sq = smem_u32(sQ);
+      const uint32_t sring = smem_u32(sRing);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t a0 = sq + t * C::TILE;
+        const uint32_t b0 = sring + kslot(j) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::SLAB + (kk & 3) * 32;
+          mma_ss(tmem + C::COL_S + t * C::BN, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
+                 kIdS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t b0 = sring + vslot(j) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          mma_ts(tmem + C::COL_O + t * D, tmem + C::COL_S + t * C::BN + kk * 8,
+                 sdesc_sw128(b0 + kk * 2048, C::SLAB, 1024), kIdPV, (j > 0 || kk > 0));
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusTimeout);
+      for (int j = 0; ok && j < n1; ++j) {
+        if (!(ok = mbar_wait(&ring_full[kslot(j)], kpar(j), abort_flag, status, kStatusTimeout))) break;
+        if (j >= 1 && !(ok = mbar_wait(&ring_full[vslot(j - 1)], vpar(j - 1), abort_flag, status, kStatusTimeout)))
+          break;
+        tc_fence_after();
+        if (j >= 1 && j - 1 < n0) {
+          if (!(ok = mbar_wait(&p_full[0], (j - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+          tc_fence_after();
+          issue_pv(0, j - 1);
+        }
+        if (j < n0) {
+          issue_s(0, j);
+          mma_commit(&s_full[0]);
+        }
+        if (j >= 1) {
+          if (!(ok = mbar_wait(&p_full[1], (j - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+          tc_fence_after();
+          issue_pv(1, j - 1);
+          mma_commit(&ring_empty[vslot(j - 1)]);
+        }
+        issue_s(1, j);
+        mma_commit(&s_full[1]);
+        mma_commit(&ring_empty[kslot(j)]);
+      }
+      if (ok) {
+        const int jl = n1 - 1;
+        ok = mbar_wait(&ring_full[vslot(jl)], vpar(jl), abort_flag, status, kStatusTimeout);
+        tc_fence_after();
+        if (ok && jl < n0) {
+          ok = mbar_wait(&p_full[0], jl & 1, abort_flag, status, kStatusTimeout);
+          tc_fence_after();
+          if (ok) issue_pv(0, jl);
+        }
+        if (ok) {
+          ok = mbar_wait(&p_full[1], jl & 1, abort_flag, status, kStatusTimeout);
+          tc_fence_after();
+          if (ok) {
+            issue_pv(1, jl);
+            mma_commit(o_full);
+          }
+        }
+      }
+      if (!ok) {  // every MMA issued so far must finish before TMEM is freed
+        mma_commit(drain);
+        drain_wait(drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp >> 2) - 1;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
+    const int row = q0 + t * C::BM + r;
+    const int n_t = t == 0 ? n0 : n1;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t tS = lane_base + C::COL_S + t * C::BN;
+    const uint32_t tO = lane_base + C::COL_O + t * D;
+
+    float m_ref = neg_inf();  // reference max, log2 units of the scaled scores
+    float l = 0.f;            // sum of exp2(score - m_ref): gives LSE
+    float l_mma = 0.f;        // the same sum over P rounded to 16 bit: normalises O
+    bool ok = true;
+    for (int j = 0; j < n_t; ++j) {
+      if (!(ok = warp_wait(&s_full[t], j & 1, abort_flag, status))) break;
+      tc_fence_after();
+      float s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+
+      const int kbase = j * C::BN;
+      const bool need_mask = (kbase + C::BN > N) || (CAUSAL && kbase + C::BN - 1 > q0 + t * C::BM);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int key = kbase + 32 * c + i;
+            if (key >= N || (CAUSAL && key > row)) s[c][i] = neg_inf();
+          }
+      }
+      float mx = s[0][0];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) mx = max3(mx, s[c][i], s[c][i + 1]);
+      const float m_new = fmaxf(m_ref, mx * scale_log2);
+      float corr = 1.f;
+      bool rescale_o = false;
+      if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold)) {
+        const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
+        corr = ex2_approx(m_ref - m_use);
+        l *= corr;
+        l_mma *= corr;
+        rescale_o = j > 0;
+        m_ref = m_use;
+      }
+      const float neg_m = (m_ref == neg_inf()) ? 0.f : -m_ref;
+      const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+      const uint64_t nm2 = f2_pack(neg_m, neg_m);
+      uint64_t sum2 = f2_pack(0.f, 0.f);   // sum of P as computed (fp32)
+      uint64_t sumr2 = f2_pack(0.f, 0.f);  // sum of P as rounded for the MMA
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 32 scores -> 16 packed pairs -> 16 TMEM columns
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[c][2 * i], s[c][2 * i + 1]), sc2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          sum2 = f2_add(sum2, f2_pack(p0, p1));
+          pk[i] = pack2(p0, p1, BF16);
+          float r0, r1;
+          unpack2(pk[i], BF16, r0, r1);
+          sumr2 = f2_add(sumr2, f2_pack(r0, r1));
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      if (rescale_o) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait(o);
+          const uint64_t corr2 = f2_pack(corr, corr);
+          uint32_t ou[32];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float a, b;
+            f2_unpack(f2_mul(f2_pack(o[i], o[i + 1]), corr2), a, b);
+            ou[i] = __float_as_uint(a);
+            ou[i + 1] = __float_as_uint(b);
+          }
+          tmem_st32(tO + 32 * c, ou);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
+      float a, b;
+      f2_unpack(sum2, a, b);
+      l += a + b;
+      f2_unpack(sumr2, a, b);
+      l_mma += a + b;
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = warp_wait(o_full, 0, abort_flag, status);
+    if (ok) {
+      tc_fence_after();
+      // O is divided by the sum of the rounded weights that entered the MMA,
+      // so each output row stays a convex combination of V rows; the
+      // rounding of the dominant weight then cancels instead of showing up
+      // at the 16-bit resolution of P.
+      const float inv_l = 1.f / l_mma;
+      // Each thread writes its own row: D/8 16-byte chunks, contiguous in memory.
+      uint4* orow = reinterpret_cast<uint4*>(o) + ((long long)bh * N + row) * (D / 8);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tmem_ld32(tO + 32 * c, ov);
+        tmem_ld_wait(ov);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, BF16);
+        if (row < N) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) orow[4 * c + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      if (row < N) {
+        const float m_fin = (m_ref == neg_inf()) ? 0.f : m_ref;
+        lse[(long long)bh * N + row] = (m_fin + __log2f(l)) * kLn2;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int n_qblocks = (a.N + C::QT * C::BM - 1) / (C::QT * C::BM);
+  const long long grid = (long long)n_qblocks * a.BH;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.N, a.BH,
+                                                         n_qblocks, a.scale_log2, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream) {
+#define FA_FWD_CASE(DD, CC, BB) \
+  if (d == DD && causal == CC && bf16 == BB) return launch_fwd_t<DD, CC, BB>(a, stream);
+  FA_FWD_CASE(64, false, false)
+  FA_FWD_CASE(64, false, true)
+  FA_FWD_CASE(64, true, false)
+  FA_FWD_CASE(64, true, true)
+  FA_FWD_CASE(128, false, false)
+  FA_FWD_CASE(128, false, true)
+  FA_FWD_CASE(128, true, false)
+  FA_FWD_CASE(128, true, true)
+#undef FA_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

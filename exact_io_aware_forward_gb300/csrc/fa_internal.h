@@ -1,0 +1,45 @@
+// Launch interfaces between the C-ABI translation unit and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Status bits latched by kernels in the device status word.
+constexpr unsigned int kStatusTimeout = 1u;
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v;        // 3-D maps over [B*H, N, d], box {64, 128, 1}
+  void* o;                             // [B*H, N, d]
+  float* lse;                          // [B*H, N]
+  int N;
+  int BH;
+  float scale_log2;                    // scale * log2(e)
+  unsigned int* status;                // device status word
+};
+cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_do;         // box {64, BQ, 1}
+  CUtensorMap tm_k, tm_v;          // box {64, 128, 1}
+  CUtensorMap tm_dk, tm_dv;        // box {64, 128, 1}
+  const float* lse;                // [B*H, N]
+  const float* delta;              // [B*H, N]
+  float* dq_accum;                 // [B*H, N, d] float32
+  int N;
+  int BH;
+  float scale;
+  float scale_log2;
+  unsigned int* status;
+};
+int backward_q_tile(int d);  // query rows per inner iteration of the dK/dV kernel
+cudaError_t launch_backward_dkdv(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const void* dO, float* delta,
+                                       float* dq_accum, long long rows, cudaStream_t stream);
+cudaError_t launch_backward_dq_convert(int d, bool bf16, const float* dq_accum, void* dq, long long rows,
+                                       float scale, cudaStream_t stream);
+
+}  // namespace fa

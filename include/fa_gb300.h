@@ -1,0 +1,132 @@
+/*
+ * fa_gb300.h -- C ABI of the exact IO-aware attention library for GB300 (sm_103a).
+ *
+ * The operation (all entry points below compute pieces of it):
+ *
+ *   O = softmax(s * Q K^T) V,  per (batch, head), s = `scale`,
+ *
+ * evaluated tile by tile with the online-softmax recurrence: a running max
+ * m, a running sum l and an unnormalised accumulator, rescaled by
+ * exp(m_old - m_new) whenever m grows ("FlashAttention 为什么不需要存下注意力矩阵",
+ * jefxiong.cn, section 3.2; "FlashAttention V1 技术深度解析", spark.aweffr.cn,
+ * section 3.2).  The forward pass writes only O and the per-row log-sum-exp
+ * LSE = m + ln l; the backward pass recomputes every tile of P on chip from
+ * LSE (same tutorial, section 3.3) -- no N x N matrix is ever written to
+ * device memory.  Under the causal mask, key j is visible to query i iff
+ * j <= i, and key tiles that are entirely masked are skipped (same tutorial,
+ * section 3.2 and 4.5).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers are DEVICE pointers owned by the caller; the library never
+ *   allocates or frees device memory and keeps no pointer after returning.
+ *   Every device pointer must be 16-byte aligned.
+ * - Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] arrays of the
+ *   16-bit type `dtype` (FA_FP16 or FA_BF16).  LSE and D are contiguous
+ *   [B, H, N] float32 arrays.  LSE is in natural-log units of the scaled
+ *   scores: LSE_i = ln sum_j exp(s * q_i . k_j).
+ * - Supported: d in {64, 128}; N >= 1 (any N: tails are masked); B, H >= 1
+ *   with B*H*N*d < 2^31; scale finite and > 0.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *   enqueue work on it and return; nothing is written to host memory and
+ *   the host never waits.
+ * - Return value: FA_OK, or FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED before
+ *   anything is launched, or FA_ERR_CUDA if a launch failed.  A kernel that
+ *   finds a pipeline wait exceeding ~2 s gives up, returns, and latches
+ *   FA_ERR_TIMEOUT in a device status word that fa_device_status() reports.
+ * - No exceptions cross this interface; all entry points are thread-safe
+ *   (they keep no mutable host state).
+ * - Outputs must not alias inputs.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_CUDA = 3,
+  FA_ERR_TIMEOUT = 4,
+  FA_ERR_WORKSPACE = 5
+} fa_status;
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fa_status_string(int status);
+
+/*
+ * Forward pass.  Writes O [B,H,N,d] (dtype) and LSE [B,H,N] (float32).
+ * Exact softmax attention by the online-softmax recurrence (tutorial
+ * section 3.2); LSE = m + ln l is the only extra output kept for the
+ * backward pass (tutorial section 3.2, last remark, and section 3.3).
+ * q, k, v: inputs; o, lse: outputs, fully overwritten.
+ */
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                     int d, int dtype, int causal, float scale, void* stream);
+
+/*
+ * Bytes of device workspace fa_backward needs: D (B*H*N float32) followed by
+ * the float32 dQ accumulator (B*H*N*d float32), each 256-byte aligned.
+ * Linear in N.  Returns 0 for invalid sizes.
+ */
+size_t fa_backward_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass (tutorial section 3.3): with G = dO and P recomputed tile by
+ * tile as exp(s * Q K^T - LSE),
+ *   dS = P * (G V^T - D),  D_i = sum_c dO_ic O_ic  ( = rowsum(P * (G V^T)) ),
+ *   dQ = s dS K,  dK = s dS^T Q,  dV = P^T G.
+ * Runs fa_backward_preprocess, fa_backward_dkdv and fa_backward_dq_convert
+ * in that order on `stream`.  `workspace` must hold
+ * fa_backward_workspace_size(B,H,N,d) bytes (else FA_ERR_WORKSPACE); its
+ * contents on entry do not matter and are overwritten.
+ * o and lse are the forward outputs for the same q, k, v, causal and scale.
+ */
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int dtype,
+                      int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Stage 1 of the backward pass: D_i = sum_c dO_ic * O_ic in float32 (the
+ * row-sum shortcut for rowsum(P * (dO V^T)), which holds because O = P V),
+ * and dq_accum := 0.  delta: [B,H,N] float32 out; dq_accum: [B,H,N,d]
+ * float32 out.
+ */
+fa_status fa_backward_preprocess(const void* o, const void* dO, float* delta, float* dq_accum, int B, int H,
+                                 int N, int d, int dtype, void* stream);
+
+/*
+ * Stage 2: for every key tile, recompute S^T and P^T per query tile from
+ * LSE, form dP^T = V dO^T and dS^T = P^T * (dP^T - D), accumulate
+ * dV = P^T dO and dK = s dS^T Q on chip and write them (dtype), and add the
+ * per-tile dQ partials dS K (unscaled, float32) into dq_accum with atomics.
+ * Causal: query tiles entirely above the diagonal are skipped.
+ */
+fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                           const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N, int d,
+                           int dtype, int causal, float scale, void* stream);
+
+/* Stage 3: dq = scale * dq_accum, rounded to dtype. */
+fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,
+                                 float scale, void* stream);
+
+/*
+ * Waits for all work queued on `stream`, then returns and clears the device
+ * status word of the library on the current device: FA_OK, FA_ERR_TIMEOUT if
+ * a kernel gave up waiting since the last call, or FA_ERR_CUDA if the
+ * stream reports an error.  The only entry point that blocks the host.
+ */
+fa_status fa_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,84 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; argument validation rejects bad calls before any CUDA work.
+No kernel is launched here (no GPU needed)."""
+import os
+import re
+
+import pytest
+
+from exact_io_aware_forward_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_gb300.h")
+
+
+def _declared():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    from exact_io_aware_forward_gb300 import _lib
+    return _lib.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for want in ("fa_forward", "fa_backward", "fa_backward_workspace_size", "fa_status_string",
+                 "fa_device_status"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from exact_io_aware_forward_gb300 import _lib
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    from exact_io_aware_forward_gb300._lib import status_string
+    assert status_string(0) == "FA_OK"
+    for code in range(1, 6):
+        assert status_string(code).startswith("FA_ERR_")
+    assert status_string(99) == "unknown fa_status"
+
+
+def test_workspace_size_is_linear_in_n(lib):
+    ws = lib.fa_backward_workspace_size
+    assert ws(1, 1, 0, 64) == 0 and ws(1, 1, 16, 96) == 0
+    a, b = ws(2, 32, 8192, 128), ws(2, 32, 16384, 128)
+    assert a == 2 * 32 * 8192 * (4 + 4 * 128)
+    assert b == 2 * a
+
+
+@pytest.mark.parametrize("case", ["null", "bad_d", "bad_dtype", "bad_scale", "misaligned", "bad_n"])
+def test_forward_rejects_bad_arguments(lib, case):
+    ptr = 1 << 20  # aligned, never dereferenced: validation fails before any launch
+    args = dict(q=ptr, k=ptr, v=ptr, o=ptr, lse=ptr, B=1, H=1, N=16, d=64, dt=1, causal=0, scale=0.125)
+    want = 1
+    if case == "null":
+        args["q"] = None
+    elif case == "bad_d":
+        args["d"], want = 96, 2
+    elif case == "bad_dtype":
+        args["dt"], want = 7, 2
+    elif case == "bad_scale":
+        args["scale"] = float("nan")
+    elif case == "misaligned":
+        args["o"] = ptr + 2
+    elif case == "bad_n":
+        args["N"] = 0
+    rc = lib.fa_forward(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["H"],
+                        args["N"], args["d"], args["dt"], args["causal"], args["scale"], None)
+    assert rc == want
+
+
+def test_backward_rejects_small_workspace(lib):
+    ptr = 1 << 20
+    rc = lib.fa_backward(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125,
+                         ptr, 16, None)
+    assert rc == 5
