@@ -140,9 +140,10 @@ fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const vo
   const int bq = fa::backward_q_tile(d);
   fa::BwdArgs a;
   if (!make_map(&a.tm_q, q, bf16, d, N, BH, bq) || !make_map(&a.tm_do, dO, bf16, d, N, BH, bq) ||
-      !make_map(&a.tm_k, k, bf16, d, N, BH, 128) || !make_map(&a.tm_v, v, bf16, d, N, BH, 128) ||
-      !make_map(&a.tm_dk, dk, bf16, d, N, BH, 128) || !make_map(&a.tm_dv, dv, bf16, d, N, BH, 128))
+      !make_map(&a.tm_k, k, bf16, d, N, BH, 128) || !make_map(&a.tm_v, v, bf16, d, N, BH, 128))
     return FA_ERR_CUDA;
+  a.dk = dk;
+  a.dv = dv;
   a.lse = lse;
   a.delta = delta;
   a.dq_accum = dq_accum;

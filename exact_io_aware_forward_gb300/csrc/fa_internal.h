@@ -25,7 +25,8 @@ cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cuda
 struct BwdArgs {
   CUtensorMap tm_q, tm_do;         // box {64, BQ, 1}
   CUtensorMap tm_k, tm_v;          // box {64, 128, 1}
-  CUtensorMap tm_dk, tm_dv;        // box {64, 128, 1}
+  void* dk;                        // [B*H, N, d]
+  void* dv;                        // [B*H, N, d]
   const float* lse;                // [B*H, N]
   const float* delta;              // [B*H, N]
   float* dq_accum;                 // [B*H, N, d] float32
