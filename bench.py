@@ -1,0 +1,343 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = forward + backward (fa_forward, then the three backward stages
+fa_backward runs: preprocess, dK/dV, dQ convert) over one batch of the
+workload, by default the causal N=8192, d=128, bf16, B=2, H=32 problem.
+Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C4]
+    python bench.py --impl reference ...   # the float64 CPU oracle as the baseline arm
+
+Throughput convention: F = 4 B H N^2 d (halved under the causal mask);
+value = 2.5 F / (t_fwd + t_bwd) in TFLOP/s, summed over all GPUs.
+Multi-GPU (torchrun): every rank runs its own copy of the workload (its own
+heads; no collective in the data path), so per-GPU work is fixed: weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOPS (fwd, fwd+bwd) & % of GB300 dense BF16 tensor peak, N=4K–32K"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_sample(w, budget_s: float, max_heads: int):
+    """Time the float64 oracle (forward + explicit backward, S and P
+    materialised) on whole heads of the workload until `budget_s` is spent.
+    Returns (TFLOP/s in the metric's convention, heads timed, seconds, threads)."""
+    import numpy as np
+    from exact_io_aware_forward_gb300.synth import as_float64, attention_inputs
+    from oracle import attention as A
+
+    # One head at a time (B = H = 1, per-head seeds) keeps host memory bounded.
+    heads, spent = 0, 0.0
+    scale = 1.0 / math.sqrt(w.d)
+    while heads < max_heads and (heads == 0 or spent < budget_s):
+        q, k, v, do = as_float64(*attention_inputs(1, 1, w.N, w.d, w.dtype, seed=w.seed * 1000 + heads,
+                                                   k_row_scale=w.k_row_scale))
+        t0 = time.perf_counter()
+        if w.N <= 16384:
+            A.forward_head(q[0, 0], k[0, 0], v[0, 0], scale, w.causal)
+            A.backward_head(q[0, 0], k[0, 0], v[0, 0], do[0, 0], scale, w.causal)
+        else:  # bounded host memory: the same definition in 2048-row stripes
+            for r0 in range(0, w.N, 2048):
+                A.forward_head(q[0, 0], k[0, 0], v[0, 0], scale, w.causal, rows=np.arange(r0, min(w.N, r0 + 2048)))
+            A.backward_head_sampled(q[0, 0], k[0, 0], v[0, 0], do[0, 0], scale, w.causal,
+                                    np.arange(w.N), np.arange(w.N))
+        spent += time.perf_counter() - t0
+        heads += 1
+    per_head = 2.5 * w.fwd_flops() / w.heads
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return per_head * heads / spent / 1e12, heads, spent, threads
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, w, world, rank, local):
+    import torch
+
+    import exact_io_aware_forward_gb300 as fa
+    from exact_io_aware_forward_gb300.synth import workload_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = load_peaks()
+    B, H, N, d = w.B, w.H, w.N, w.d
+    q, k, v, do = (x.to(dev) for x in workload_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.fa_backward_workspace_size(B, H, N, d), device=dev, dtype=torch.uint8)
+    rows = B * H * N
+    delta = ws[: rows * 4].view(torch.float32).view(B, H, N)
+    off = (rows * 4 + 255) // 256 * 256
+    acc = ws[off: off + rows * d * 4].view(torch.float32).view(B, H, N, d)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+
+    def step(e=None):
+        # The same four launches fa_backward makes, split so that each kernel is timed.
+        if e: e[0].record(stream)
+        fa.fa_forward(q, k, v, o, lse, w.causal)
+        if e: e[1].record(stream)
+        fa.fa_backward_preprocess(o, do, delta, acc)
+        if e: e[2].record(stream)
+        fa.fa_backward_dkdv(q, k, v, do, lse, delta, acc, dk, dv, w.causal)
+        if e: e[3].record(stream)
+        fa.fa_backward_dq_convert(acc, dq)
+        if e: e[4].record(stream)
+
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem_inputs = torch.cuda.memory_allocated(dev)
+    for _ in range(args.warmup):
+        step()
+    fa.fa_device_status()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    fa.fa_device_status()
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+    total_ms = t0.elapsed_time(t1)
+    parts = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps for j in range(4)]
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    F = w.fwd_flops()
+    value = world * 2.5 * F / (ms_step * 1e-3) / 1e12
+
+    # End to end through the public API: pinned host inputs in, results out.
+    hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+    ho, hdq, hdk, hdv = (torch.empty_like(x, device="cpu").pin_memory() for x in (q, q, q, q))
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        gq, gk, gv, gdo = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, hdo))
+        go, glse = fa.forward(gq, gk, gv, causal=w.causal)
+        gdq, gdk, gdv = fa.backward(gq, gk, gv, go, glse, gdo, causal=w.causal, workspace=ws)
+        for h, g in ((ho, go), (hlse, glse), (hdq, gdq), (hdk, gdk), (hdv, gdv)):
+            h.copy_(g, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    if dist:
+        dist.barrier()
+    c0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - c0) * 1e3 / e2e_steps
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    fa.fa_device_status()
+    elem = B * H * N * d * 2
+    h2d = 4 * elem
+    d2h = 4 * elem + B * H * N * 4
+
+    result = None
+    if rank == 0:
+        peak = float(peaks["bf16_tflops"])
+        dkdv_tflops = 2.5 * F / (parts[2] * 1e-3) / 1e12
+        fwd_tflops = F / (parts[0] * 1e-3) / 1e12
+        bwd_ms = parts[1] + parts[2] + parts[3]
+        naive_sp = 2 * N * N * 2 * B * H
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded N(0,1) Q, K, V, dO; no dataset)",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                       "global_batch": B * world, "seq_len": N, "parallelism": f"independent heads x{world}",
+                       "flop_count": "fwd+bwd = 2.5 * 4*B*H*N^2*d (halved causal)",
+                       "l2": "inputs larger than L2 (each of Q, K, V, dO is %.0f MB > 129 MB)" % (elem / 1e6)},
+            "fwd_tflops": round(fwd_tflops, 1), "fwd_frac_of_peak": round(fwd_tflops / peak, 4),
+            "fwdbwd_frac_of_peak": round(value / world / peak, 4),
+            "fwdbwd_tflops_3p5F": round(3.5 * F / (ms_step * 1e-3) / 1e12, 1),
+            "bwd_tflops_2p5F": round(2.5 * F / (bwd_ms * 1e-3) / 1e12, 1),
+            "kernel_ms": {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
+                          "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)},
+            "roofline": {"bound": "tensor", "kernel": "fa_bwd_dkdv_kernel<128,causal,bf16>",
+                         "achieved": round(dkdv_tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(dkdv_tflops / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "algorithmic": "10*N^2*d per head (5 GEMMs), halved causal, per launch"},
+            "peak_memory_bytes": int(peak_mem), "inputs_bytes": int(mem_inputs),
+            "naive_sp_bytes": int(naive_sp),
+            "e2e": {"value": round(world * 2.5 * F / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": round(e2e_ms, 3)},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+        }
+    if dist:
+        dist.destroy_process_group()
+    return result
+
+
+def run_reference(args, w, world, rank):
+    """The float64 CPU oracle as the baseline arm: each step is a bounded
+    sample (whole heads of the same workload) on the host cores."""
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0, 1)
+    vals, heads_total, spent_total, threads = [], 0, 0.0, 1
+    for _ in range(args.steps):
+        v, heads, spent, threads = oracle_sample(w, 0.0, 1)
+        vals.append(v)
+        heads_total += heads
+        spent_total += spent
+    value = heads_total * 2.5 * w.fwd_flops() / w.heads / spent_total / 1e12
+    sample = f"{heads_total} whole head(s) of {w.name} over {args.steps} steps, float64 NumPy oracle"
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(spent_total * 1e3 / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="C4", help="C2, C3N, C3C, C4 or C5")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing (rank 0, N=1)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    from exact_io_aware_forward_gb300.synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, w, world, rank)
+    else:
+        from exact_io_aware_forward_gb300 import build as fa_build
+        fa_build.build()
+        out = run_gpu(args, w, world, rank, local)
+        if out is not None and world == 1:
+            v, heads, spent, threads = oracle_sample(w, args.cpu_budget, 64)
+            out["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                   "sample": f"{heads} whole head(s) of {w.name} (N={w.N}, d={w.d}), "
+                                             f"float64 forward + explicit backward, {spent:.1f} s"}
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()
