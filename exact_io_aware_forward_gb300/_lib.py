@@ -25,6 +25,7 @@ SIGNATURES = {
     "fa_backward_preprocess": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "fa_backward_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_backward_dq_convert": (_I, [_P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_device_status": (_I, [_P]),
 }
 

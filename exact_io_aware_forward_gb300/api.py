@@ -93,6 +93,21 @@ def fa_backward(q, k, v, o, do, lse, dq, dk, dv, workspace, causal=False, scale=
                                             _stream(stream)))
 
 
+def fa_backward_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal=False, scale=None, stream=None) -> None:
+    """fa_backward without a workspace: the library's fixed device scratch
+    (32 MiB per GPU) holds D and the dQ accumulator.  For callers that cannot
+    allocate device memory.  Calls that overlap on the GPU share that scratch
+    and must be serialised; the first call on a device must precede any
+    stream capture."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("o", o, q.shape, dt),
+            _bhnd("do", do, q.shape, dt), _bhnd("lse", lse, (B, H, N), torch.float32),
+            _bhnd("dq", dq, q.shape, dt), _bhnd("dk", dk, q.shape, dt), _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_noalloc", lib().fa_backward_noalloc(*args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)),
+                                                            _scale(scale, d), _stream(stream)))
+
+
 def fa_backward_preprocess(o, do, delta, dq_accum, stream=None) -> None:
     B, H, N, d = _shape(o)
     dt = o.dtype

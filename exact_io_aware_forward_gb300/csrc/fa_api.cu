@@ -79,6 +79,8 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA launch or the stream failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up waiting on its pipeline";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case FA_ERR_SCRATCH_TOO_SMALL:
+      return "FA_ERR_SCRATCH_TOO_SMALL: fa_backward_noalloc needs more than its fixed 32 MiB scratch; use fa_backward";
     default: return "unknown fa_status";
   }
 }

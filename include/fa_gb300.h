@@ -53,7 +53,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,
   FA_ERR_CUDA = 3,
   FA_ERR_TIMEOUT = 4,
-  FA_ERR_WORKSPACE = 5
+  FA_ERR_WORKSPACE = 5,
+  FA_ERR_SCRATCH_TOO_SMALL = 6
 } fa_status;
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
@@ -116,6 +117,31 @@ fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const vo
 /* Stage 3: dq = scale * dq_accum, rounded to dtype. */
 fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,
                                  float scale, void* stream);
+
+/*
+ * Size of the fixed device scratch array used by fa_backward_noalloc.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * fa_backward without a workspace argument, for callers that cannot
+ * allocate device memory (plugins inside a framework that owns every
+ * allocation, allocation-free serving paths, callers that only hold raw
+ * input/output pointers).  The pages have no counterpart: this is a
+ * deployment convenience, computing exactly what fa_backward computes.
+ * The D vector and the fp32 dQ accumulator live in a static device array of
+ * FA_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading the library keeps
+ * until the process exits.  Problems with fa_backward_workspace_size() larger
+ * than that return FA_ERR_SCRATCH_TOO_SMALL before any launch.  The first
+ * call on a device looks up the array's address with that device current;
+ * make it before any stream capture starts.  All calls share the array:
+ * calls that overlap on the GPU race and must be serialised.  Each call
+ * rewrites D and zeroes the accumulator, so stale contents do not matter.
+ * Other arguments, ownership and errors: as fa_backward.
+ */
+fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                              int dtype, int causal, float scale, void* stream);
 
 /*
  * Waits for all work queued on `stream`, then returns and clears the device
