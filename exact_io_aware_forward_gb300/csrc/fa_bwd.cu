@@ -21,13 +21,18 @@
 //     double-buffered in TMEM and added into the float32 dq_accum with
 //     vector/scalar reductions (red.global.add) by a separate warpgroup.
 //
-// Warp roles (384 threads):
-//   warp 0      TMA: K, V once; Q_i, dO_i through a 2-stage ring.
-//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma.  The S^T
-//               and dP^T of tile i+1 are issued as soon as the compute
-//               warps have pulled tile i's into registers, so the tensor
-//               core works on tile i+1 while tile i's P and dS are formed.
-//   warps 4-7   compute: one key row per thread (TMEM lane).
+// Warp roles (512 threads):
+//   warp 0      TMA: K, V once; Q_i, dO_i through a 4-stage ring (3 at d = 64).
+//   warps 1-3   TMEM allocation (warp 1); lane 0 of each issues part of the
+//               tcgen05.mma work (one thread can only issue about one MMA per
+//               ~100 cycles).  The S^T and dP^T of tile i+1 are issued as soon
+//               as the compute warps have pulled tile i's into registers, so
+//               the tensor core works on tile i+1 while tile i's P and dS
+//               are formed.
+//   warps 4-7, 12-15  compute: one key row per thread (TMEM lane), each
+//               warpgroup on half of the query columns; P^T / dS^T have one
+//               shared-memory buffer, written after the math of the next
+//               tile once the previous tile's products are done.
 //   warps 8-11  dQ drain, then half of the epilogue.
 // Causal: query tiles entirely above the diagonal are skipped by the loop
 // bounds (the whole-block skip of section 4.5); the diagonal tile is
@@ -58,21 +63,22 @@ struct BwdCfg {
   static constexpr int Q_TILE = SLABS * Q_SLAB;
   static constexpr int PT_SLAB = BKV * 128;         // 128 key rows x 64 query cols
   static constexpr int PT_TILE = (BQ / 64) * PT_SLAB;
-  static constexpr int PS = D == 128 ? 2 : 1;       // P^T / dS^T buffers
+  static constexpr int PS = 1;                      // P^T / dS^T buffers
+  static constexpr int QS = D == 128 ? 4 : 3;       // Q / dO stages
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
-  static constexpr int OFF_Q = OFF_V + KV_TILE;     // [2] stages
-  static constexpr int OFF_DO = OFF_Q + 2 * Q_TILE;
-  static constexpr int OFF_P = OFF_DO + 2 * Q_TILE; // [PS]
+  static constexpr int OFF_Q = OFF_V + KV_TILE;     // [QS] stages
+  static constexpr int OFF_DO = OFF_Q + QS * Q_TILE;
+  static constexpr int OFF_P = OFF_DO + QS * Q_TILE; // [PS]
   static constexpr int OFF_DS = OFF_P + PS * PT_TILE;
   static constexpr int OFF_LD = OFF_DS + PS * PT_TILE;  // [2][2][BQ] floats: LSE*log2e, D
   static constexpr int OFF_BAR = OFF_LD + 2 * 2 * BQ * 4;
-  // kv_full, q_full[2], q_empty[2], sdp_full, sdp_empty, pds_full[PS], pds_empty[PS],
-  // dq_full[2], dq_empty[2], ld_full[2], dkdv_full, drain
-  static constexpr int NBAR = 1 + 2 + 2 + 1 + 1 + 2 * PS + 2 + 2 + 2 + 1 + 1;
+  // kv_full, q_full[QS], q_empty[QS], sdp_full, sdp_empty, pds_full[PS], pds_empty[PS],
+  // dq_full[2], dq_empty[2], ld_full[2], dkdv_full, drain[3]
+  static constexpr int NBAR = 1 + 2 * QS + 1 + 1 + 2 * PS + 2 + 2 + 2 + 1 + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 512;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 0;
   static constexpr uint32_t COL_DP = BQ;
@@ -135,7 +141,7 @@ __device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint4* dst,
 }
 
 template <int D, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        void* __restrict__ dk, void* __restrict__ dv, const float* __restrict__ lse,
@@ -156,8 +162,8 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* q_full = kv_full + 1;
-  uint64_t* q_empty = q_full + 2;
-  uint64_t* sdp_full = q_empty + 2;
+  uint64_t* q_empty = q_full + C::QS;
+  uint64_t* sdp_full = q_empty + C::QS;
   uint64_t* sdp_empty = sdp_full + 1;
   uint64_t* pds_full = sdp_empty + 1;
   uint64_t* pds_empty = pds_full + C::PS;
@@ -171,9 +177,12 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Heaviest first under the causal mask: key tile 0 sees every query tile.
-  const int bh = blockIdx.x % BH;
-  const int j = blockIdx.x / BH;
+  // Head-major order: the CTAs of one head run together, so its Q, dO and
+  // float32 dQ accumulator stay in L2; within a head key tile 0 (which sees
+  // every query tile under the causal mask) goes first.
+  const int n_kvt = (N + C::BKV - 1) / C::BKV;
+  const int bh = blockIdx.x / n_kvt;
+  const int j = blockIdx.x % n_kvt;
   const int kv0 = j * C::BKV;
   const int n_q = (N + BQ - 1) / BQ;
   const int i_begin = CAUSAL ? kv0 / BQ : 0;
@@ -182,21 +191,23 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::QS; ++b) {
       mbar_init(&q_full[b], 1);
       mbar_init(&q_empty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&dq_full[b], 1);
       mbar_init(&dq_empty[b], 4);
-      mbar_init(&ld_full[b], 4);
+      mbar_init(&ld_full[b], 8);
     }
-    mbar_init(sdp_full, 1);
-    mbar_init(sdp_empty, 4);
+    mbar_init(sdp_full, 2);
+    mbar_init(sdp_empty, 8);
     for (int b = 0; b < C::PS; ++b) {
-      mbar_init(&pds_full[b], 4);
-      mbar_init(&pds_empty[b], 1);
+      mbar_init(&pds_full[b], 8);
+      mbar_init(&pds_empty[b], 2);
     }
     mbar_init(dkdv_full, 1);
-    mbar_init(drain, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&drain[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -225,8 +236,8 @@ __global__ void __launch_bounds__(384, 1)
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int b = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1);
+        const int b = it % C::QS;
+        const uint32_t use = (uint32_t)(it / C::QS);
         if (!mbar_wait(&q_empty[b], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         mbar_arrive_expect_tx(&q_full[b], 2 * C::Q_TILE);
         const int q0 = (i_begin + it) * BQ;
@@ -238,12 +249,17 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (*abort_flag) {  // let every copy in flight land before the CTA exits
         drain_wait(kv_full, 0);
-        for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
-          drain_wait(&q_full[it & 1], (uint32_t)((it >> 1) & 1));
+        for (int it = issued - C::QS < 0 ? 0 : issued - C::QS; it < issued; ++it)
+          drain_wait(&q_full[it % C::QS], (uint32_t)((it / C::QS) & 1));
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= 1 && warp <= 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // A single thread issues at most one tcgen05.mma every ~100 cycles, so
+    // the five products are spread over three issuing threads:
+    //   warp 1: S^T(i+1) = K Q^T, then the dQ partial of tile i
+    //   warp 2: dP^T(i+1) = V dO^T
+    //   warp 3: dV += P^T dO, dK += dS^T Q of tile i
     if (lane == 0) {
       constexpr uint32_t kIdSdP = idesc_f16(128, BQ, BF16, false, false);   // K-major A, K-major B
       constexpr uint32_t kIdAcc = idesc_f16(128, D, BF16, false, true);     // K-major A, MN-major B
@@ -251,83 +267,98 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
       const uint32_t aP = smem_u32(sP), aDS = smem_u32(sDS);
-      // S^T = K Q^T and dP^T = V dO^T for the query tile in stage b.
-      auto issue_sdp = [&](int b) {
+      // S^T = K Q^T (warp 1) or dP^T = V dO^T (warp 2) for the tile in stage qs.
+      auto issue_sdp = [&](int qs) {
+        const uint64_t da = sdesc_sw128(warp == 1 ? aK : aV, 16, 1024);
+        const uint64_t db = sdesc_sw128((warp == 1 ? aQ : aDO) + qs * C::Q_TILE, 16, 1024);
+        const uint32_t dcol = tmem + (warp == 1 ? C::COL_S : C::COL_DP);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ok = (kk >> 2) * C::KV_SLAB + (kk & 3) * 32;
-          const uint32_t oq = b * C::Q_TILE + (kk >> 2) * C::Q_SLAB + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S, sdesc_sw128(aK + ok, 16, 1024), sdesc_sw128(aQ + oq, 16, 1024), kIdSdP, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ok = (kk >> 2) * C::KV_SLAB + (kk & 3) * 32;
-          const uint32_t oq = b * C::Q_TILE + (kk >> 2) * C::Q_SLAB + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_DP, sdesc_sw128(aV + ok, 16, 1024), sdesc_sw128(aDO + oq, 16, 1024), kIdSdP,
-                 kk > 0);
+          const uint32_t ok = ((kk >> 2) * C::KV_SLAB + (kk & 3) * 32) >> 4;
+          const uint32_t oq = ((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
+          mma_ss(dcol, da + ok, db + oq, kIdSdP, kk > 0);
         }
       };
-      // dV += P^T dO, dK += dS^T Q (stage b, P/dS buffer pb), dQ partial -> buffer b.
-      auto issue_acc = [&](int b, int pb, bool first) {
+      // dV += P^T dO and dK += dS^T Q (warp 3).
+      auto issue_dkdv = [&](int qs, int pb, bool first) {
+        const uint64_t dp = sdesc_sw128(aP + pb * C::PT_TILE, 16, 1024);
+        const uint64_t dds = sdesc_sw128(aDS + pb * C::PT_TILE, 16, 1024);
+        const uint64_t ddo = sdesc_sw128(aDO + qs * C::Q_TILE, C::Q_SLAB, 1024);
+        const uint64_t dq = sdesc_sw128(aQ + qs * C::Q_TILE, C::Q_SLAB, 1024);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t op = pb * C::PT_TILE + (kk >> 2) * C::PT_SLAB + (kk & 3) * 32;
-          const uint32_t oq = b * C::Q_TILE + kk * 2048;
-          mma_ss(tmem + C::COL_DV, sdesc_sw128(aP + op, 16, 1024), sdesc_sw128(aDO + oq, C::Q_SLAB, 1024), kIdAcc,
-                 !(first && kk == 0));
+          const uint32_t op = ((kk >> 2) * C::PT_SLAB + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_DV, dp + op, ddo + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
         }
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t op = pb * C::PT_TILE + (kk >> 2) * C::PT_SLAB + (kk & 3) * 32;
-          const uint32_t oq = b * C::Q_TILE + kk * 2048;
-          mma_ss(tmem + C::COL_DK, sdesc_sw128(aDS + op, 16, 1024), sdesc_sw128(aQ + oq, C::Q_SLAB, 1024), kIdAcc,
-                 !(first && kk == 0));
+          const uint32_t op = ((kk >> 2) * C::PT_SLAB + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_DK, dds + op, dq + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
         }
+      };
+      // dQ partial -> TMEM buffer b (warp 1).
+      auto issue_dq = [&](int pb, int b) {
+        const uint64_t dk0 = sdesc_sw128(aK, C::KV_SLAB, 1024);
+        const uint64_t ds0 = sdesc_sw128(aDS + pb * C::PT_TILE, C::PT_SLAB, 1024);
 #pragma unroll
         for (int kk = 0; kk < C::BKV / 16; ++kk) {
-          const uint64_t dk_desc = sdesc_sw128(aK + kk * 2048, C::KV_SLAB, 1024);
-          const uint64_t ds_desc = sdesc_sw128(aDS + pb * C::PT_TILE + kk * 2048, C::PT_SLAB, 1024);
+          const uint32_t o = (kk * 2048) >> 4;
           if (C::DQT)  // dQ^T = K^T dS^T
-            mma_ss(tmem + C::COL_DQ + 64 * b, dk_desc, ds_desc, kIdDq, kk > 0);
+            mma_ss(tmem + C::COL_DQ + 64 * b, dk0 + o, ds0 + o, kIdDq, kk > 0);
           else         // dQ = dS K
-            mma_ss(tmem + C::COL_DQ + 64 * b, ds_desc, dk_desc, kIdDq, kk > 0);
+            mma_ss(tmem + C::COL_DQ + 64 * b, ds0 + o, dk0 + o, kIdDq, kk > 0);
         }
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag, status, kStatusTimeout);
-      if (ok) ok = mbar_wait(&q_full[0], 0, abort_flag, status, kStatusTimeout);
-      if (ok) {
-        tc_fence_after();
-        issue_sdp(0);
-        mma_commit(sdp_full);
+      if (warp <= 2) {
+        if (ok) ok = mbar_wait(&q_full[0], 0, abort_flag, status, kStatusTimeout);
+        if (ok) {
+          tc_fence_after();
+          issue_sdp(0);
+          mma_commit(sdp_full);
+        }
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int b = it & 1;
+        const int qs = it % C::QS;
         const int pb = it % C::PS;
-        if (it + 1 < n_it) {
+        if (warp <= 2 && it + 1 < n_it) {
+          const int qn = (it + 1) % C::QS;
           if (!(ok = mbar_wait(sdp_empty, it & 1, abort_flag, status, kStatusTimeout))) break;
-          if (!(ok = mbar_wait(&q_full[b ^ 1], ((it + 1) >> 1) & 1, abort_flag, status, kStatusTimeout))) break;
+          if (!(ok = mbar_wait(&q_full[qn], ((it + 1) / C::QS) & 1, abort_flag, status, kStatusTimeout))) break;
           tc_fence_after();
-          issue_sdp(b ^ 1);
+          issue_sdp(qn);
           mma_commit(sdp_full);
         }
+        if (warp == 2) continue;
         if (!(ok = mbar_wait(&pds_full[pb], (it / C::PS) & 1, abort_flag, status, kStatusTimeout))) break;
-        if (!(ok = mbar_wait(&dq_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, status, kStatusTimeout))) break;
-        tc_fence_after();
-        issue_acc(b, pb, it == 0);
-        mma_commit(&dq_full[b]);
-        mma_commit(&pds_empty[pb]);
-        mma_commit(&q_empty[b]);
+        if (warp == 1) {
+          if (!(ok = mbar_wait(&dq_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, status, kStatusTimeout))) break;
+          tc_fence_after();
+          issue_dq(pb, b);
+          mma_commit(&dq_full[b]);
+          mma_commit(&pds_empty[pb]);
+        } else {
+          tc_fence_after();
+          issue_dkdv(qs, pb, it == 0);
+          mma_commit(&pds_empty[pb]);
+          mma_commit(&q_empty[qs]);
+        }
       }
-      if (ok) mma_commit(dkdv_full);
-      else {  // every MMA issued so far must finish before TMEM is freed
-        mma_commit(drain);
-        drain_wait(drain, 0);
+      if (ok && warp == 3) mma_commit(dkdv_full);
+      if (!ok) {  // every MMA this thread issued must finish before TMEM is freed
+        mma_commit(&drain[warp - 1]);
+        drain_wait(&drain[warp - 1], 0);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // ------------------------------------------------------------ compute: P^T, dS^T
+    // Warpgroup h = 0 (warps 4-7) owns query columns [0, CW) of every tile,
+    // h = 1 (warps 12-15) owns [CW, BQ); one key row per thread (TMEM lane).
+    constexpr int CW = BQ / 2;
+    const int h = warp >= 12 ? 1 : 0;
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // key row within the tile == TMEM lane
+    const int r = quarter * 32 + lane;
     const int key = kv0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
@@ -335,8 +366,8 @@ __global__ void __launch_bounds__(384, 1)
     // and -D, staged in shared memory one iteration ahead.
     float pre_l = 0.f, pre_d = 0.f;
     auto fetch = [&](int it) {
-      const int q = (i_begin + it) * BQ + r;
-      if (r < BQ) {
+      const int q = (i_begin + it) * BQ + h * CW + r;
+      if (r < CW) {
         if (q < N) {
           pre_l = -lse[head_row + q] * kLog2e;
           pre_d = -delta[head_row + q];
@@ -353,9 +384,9 @@ __global__ void __launch_bounds__(384, 1)
       const int pb = it % C::PS;
       float* sNL = sLD + lb * 2 * BQ;
       float* sND = sNL + BQ;
-      if (r < BQ) {
-        sNL[r] = pre_l;
-        sND[r] = pre_d;
+      if (r < CW) {
+        sNL[h * CW + r] = pre_l;
+        sND[h * CW + r] = pre_d;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ld_full[lb]);
@@ -365,51 +396,49 @@ __global__ void __launch_bounds__(384, 1)
       if (!(ok = warp_wait(sdp_full, it & 1, abort_flag, status))) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int ch = 0; ch < BQ / 64; ++ch) {
-        float s[2][32], dp[2][32];
-        tmem_ld32(lane_base + C::COL_S + 64 * ch, s[0]);
-        tmem_ld32(lane_base + C::COL_S + 64 * ch + 32, s[1]);
-        tmem_ld32(lane_base + C::COL_DP + 64 * ch, dp[0]);
-        tmem_ld32(lane_base + C::COL_DP + 64 * ch + 32, dp[1]);
-        tmem_ld_wait(s[0]);
-        tmem_ld_wait(s[1]);
-        tmem_ld_wait(dp[0]);
-        tmem_ld_wait(dp[1]);
-        if (ch == BQ / 64 - 1) {  // S^T / dP^T columns may now be overwritten by the next tile
+      for (int sc = 0; sc < CW / 32; ++sc) {
+        const int col = h * CW + 32 * sc;  // first column of this 32-column sub-chunk
+        float s[32], dp[32];
+        tmem_ld32(lane_base + C::COL_S + col, s);
+        tmem_ld32(lane_base + C::COL_DP + col, dp);
+        tmem_ld_wait(s);
+        tmem_ld_wait(dp);
+        if (sc == CW / 32 - 1) {  // S^T / dP^T columns may now be overwritten by the next tile
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(sdp_empty);
         }
-        if (ch == 0 && !(ok = warp_wait(&pds_empty[pb], ((it / C::PS) & 1) ^ 1, abort_flag, status))) break;
-        const int c0 = q0 + 64 * ch;  // first query of this chunk
+        const int c0 = q0 + col;  // first query of this sub-chunk
         const bool need_mask = (CAUSAL && c0 < kv0 + C::BKV - 1) || (kv0 + C::BKV > N);
-        uint32_t pp[32], dd[32];
+        uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
           const int c = 2 * i;
-          const float2 nl = *reinterpret_cast<const float2*>(sNL + 64 * ch + c);
-          const float2 nd = *reinterpret_cast<const float2*>(sND + 64 * ch + c);
+          const float2 nl = *reinterpret_cast<const float2*>(sNL + col + c);
+          const float2 nd = *reinterpret_cast<const float2*>(sND + col + c);
           float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[c >> 5][c & 31], s[c >> 5][(c & 31) + 1]), sc2, f2_pack(nl.x, nl.y)), x0, x1);
+          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, f2_pack(nl.x, nl.y)), x0, x1);
           float p0 = ex2_approx(x0);
           float p1 = ex2_approx(x1);
           if (need_mask) {
             if (key >= N || (CAUSAL && key > c0 + c)) p0 = 0.f;
             if (key >= N || (CAUSAL && key > c0 + c + 1)) p1 = 0.f;
           }
-          const uint64_t t2 = f2_add(f2_pack(dp[c >> 5][c & 31], dp[c >> 5][(c & 31) + 1]), f2_pack(nd.x, nd.y));
+          const uint64_t t2 = f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(nd.x, nd.y));
           float d0, d1;
           f2_unpack(f2_mul(f2_pack(p0, p1), t2), d0, d1);
           pp[i] = pack2(p0, p1, BF16);
           dd[i] = pack2(d0, d1, BF16);
         }
-        uint8_t* prow = sP + pb * C::PT_TILE + ch * C::PT_SLAB;
-        uint8_t* drow = sDS + pb * C::PT_TILE + ch * C::PT_SLAB;
+        // The buffer is free once the products of the previous tile are done.
+        if (sc == 0 && !(ok = warp_wait(&pds_empty[pb], ((it / C::PS) & 1) ^ 1, abort_flag, status))) break;
+        uint8_t* prow = sP + pb * C::PT_TILE + (col >> 6) * C::PT_SLAB;
+        uint8_t* drow = sDS + pb * C::PT_TILE + (col >> 6) * C::PT_SLAB;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          *reinterpret_cast<uint4*>(prow + sw128_offset(r, 8 * q)) =
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint4*>(prow + sw128_offset(r, (col & 63) + 8 * q)) =
               make_uint4(pp[4 * q], pp[4 * q + 1], pp[4 * q + 2], pp[4 * q + 3]);
-          *reinterpret_cast<uint4*>(drow + sw128_offset(r, 8 * q)) =
+          *reinterpret_cast<uint4*>(drow + sw128_offset(r, (col & 63) + 8 * q)) =
               make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
         }
       }
@@ -418,13 +447,15 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&pds_full[pb]);
     }
-    if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
-    if (ok) {
-      tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(dv) + (head_row + key) * (D / 8);
-      store_rows_from_tmem<D, BF16>(lane_base + C::COL_DV, dst, key < N, 1.f);
+    if (h == 0) {
+      if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
+      if (ok) {
+        tc_fence_after();
+        uint4* dst = reinterpret_cast<uint4*>(dv) + (head_row + key) * (D / 8);
+        store_rows_from_tmem<D, BF16>(lane_base + C::COL_DV, dst, key < N, 1.f);
+      }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------ dQ drain
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
