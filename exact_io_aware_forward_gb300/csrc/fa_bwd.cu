@@ -21,7 +21,7 @@
 //     double-buffered in TMEM and added into the float32 dq_accum with
 //     vector/scalar reductions (red.global.add) by a separate warpgroup.
 //
-// Warp roles (512 threads):
+// Warp roles (640 threads):
 //   warp 0      TMA: K, V once; Q_i, dO_i through a 4-stage ring (3 at d = 64).
 //   warps 1-3   TMEM allocation (warp 1); lane 0 of each issues part of the
 //               tcgen05.mma work (one thread can only issue about one MMA per
@@ -30,10 +30,14 @@
 //               the tensor core works on tile i+1 while tile i's P and dS
 //               are formed.
 //   warps 4-7, 12-15  compute: one key row per thread (TMEM lane), each
-//               warpgroup on half of the query columns; P^T / dS^T have one
-//               shared-memory buffer, written after the math of the next
-//               tile once the previous tile's products are done.
-//   warps 8-11  dQ drain, then half of the epilogue.
+//               warpgroup on half of the query columns.  P^T and dS^T have
+//               one buffer each (TMEM at d = 128, where dV and dK then read
+//               their A operand from TMEM; shared memory at d = 64; dS^T is
+//               always in shared memory too, as an operand of the dQ
+//               product), written after the math of the next tile once the
+//               previous tile's products are done.
+//   warps 8-11, 16-19  dQ drain (each warpgroup half of the columns), then
+//               half of the epilogue.
 // Causal: query tiles entirely above the diagonal are skipped by the loop
 // bounds (the whole-block skip of section 4.5); the diagonal tile is
 // masked elementwise.
@@ -65,12 +69,16 @@ struct BwdCfg {
   static constexpr int PT_TILE = (BQ / 64) * PT_SLAB;
   static constexpr int PS = 1;                      // P^T / dS^T buffers
   static constexpr int QS = D == 128 ? 4 : 3;       // Q / dO stages
+  // d = 128: P^T and dS^T also go to TMEM (A operands of dV and dK read from
+  // TMEM, saving shared-memory bandwidth); dQ then has one TMEM buffer.
+  static constexpr bool PT_TMEM = D == 128;
+  static constexpr int DQB = PT_TMEM ? 1 : 2;       // dQ TMEM buffers
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
   static constexpr int OFF_Q = OFF_V + KV_TILE;     // [QS] stages
   static constexpr int OFF_DO = OFF_Q + QS * Q_TILE;
   static constexpr int OFF_P = OFF_DO + QS * Q_TILE; // [PS]
-  static constexpr int OFF_DS = OFF_P + PS * PT_TILE;
+  static constexpr int OFF_DS = OFF_P + (PT_TMEM ? 0 : PS * PT_TILE);
   static constexpr int OFF_LD = OFF_DS + PS * PT_TILE;  // [2][2][BQ] floats: LSE*log2e, D
   static constexpr int OFF_BAR = OFF_LD + 2 * 2 * BQ * 4;
   // kv_full, q_full[QS], q_empty[QS], sdp_full, sdp_empty, pds_full[PS], pds_empty[PS],
@@ -78,12 +86,14 @@ struct BwdCfg {
   static constexpr int NBAR = 1 + 2 * QS + 1 + 1 + 2 * PS + 2 + 2 + 2 + 1 + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
-  static constexpr int THREADS = 512;
+  static constexpr int THREADS = 640;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S = 0;
   static constexpr uint32_t COL_DP = BQ;
-  static constexpr uint32_t COL_DQ = 2 * BQ;        // two buffers of 64 columns
-  static constexpr uint32_t COL_DV = 2 * BQ + 128;
+  static constexpr uint32_t COL_DQ = 2 * BQ;        // DQB buffers of 64 columns
+  static constexpr uint32_t COL_PT = COL_DQ + 64 * DQB;      // P^T, 16-bit pairs (PT_TMEM)
+  static constexpr uint32_t COL_DST = COL_PT + BQ / 2;       // dS^T, 16-bit pairs (PT_TMEM)
+  static constexpr uint32_t COL_DV = PT_TMEM ? COL_DST + BQ / 2 : COL_DQ + 128;
   static constexpr uint32_t COL_DK = COL_DV + D;
   static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -141,7 +151,7 @@ __device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint4* dst,
 }
 
 template <int D, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(640, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        void* __restrict__ dk, void* __restrict__ dv, const float* __restrict__ lse,
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dq_full[b], 1);
-      mbar_init(&dq_empty[b], 4);
+      mbar_init(&dq_empty[b], 8);
       mbar_init(&ld_full[b], 8);
     }
     mbar_init(sdp_full, 2);
@@ -279,7 +289,7 @@ __global__ void __launch_bounds__(512, 1)
           mma_ss(dcol, da + ok, db + oq, kIdSdP, kk > 0);
         }
       };
-      // dV += P^T dO and dK += dS^T Q (warp 3).
+      // dV += P^T dO and dK += dS^T Q (warp 3); A from TMEM when PT_TMEM.
       auto issue_dkdv = [&](int qs, int pb, bool first) {
         const uint64_t dp = sdesc_sw128(aP + pb * C::PT_TILE, 16, 1024);
         const uint64_t dds = sdesc_sw128(aDS + pb * C::PT_TILE, 16, 1024);
@@ -288,12 +298,18 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t op = ((kk >> 2) * C::PT_SLAB + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_DV, dp + op, ddo + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
+          if (C::PT_TMEM)
+            mma_ts(tmem + C::COL_DV, tmem + C::COL_PT + kk * 8, ddo + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
+          else
+            mma_ss(tmem + C::COL_DV, dp + op, ddo + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
         }
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t op = ((kk >> 2) * C::PT_SLAB + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_DK, dds + op, dq + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
+          if (C::PT_TMEM)
+            mma_ts(tmem + C::COL_DK, tmem + C::COL_DST + kk * 8, dq + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
+          else
+            mma_ss(tmem + C::COL_DK, dds + op, dq + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
         }
       };
       // dQ partial -> TMEM buffer b (warp 1).
@@ -319,7 +335,7 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
       for (int it = 0; ok && it < n_it; ++it) {
-        const int b = it & 1;
+        const int b = it % C::DQB;
         const int qs = it % C::QS;
         const int pb = it % C::PS;
         if (warp <= 2 && it + 1 < n_it) {
@@ -333,7 +349,7 @@ __global__ void __launch_bounds__(512, 1)
         if (warp == 2) continue;
         if (!(ok = mbar_wait(&pds_full[pb], (it / C::PS) & 1, abort_flag, status, kStatusTimeout))) break;
         if (warp == 1) {
-          if (!(ok = mbar_wait(&dq_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, status, kStatusTimeout))) break;
+          if (!(ok = mbar_wait(&dq_empty[b], ((it / C::DQB) & 1) ^ 1, abort_flag, status, kStatusTimeout))) break;
           tc_fence_after();
           issue_dq(pb, b);
           mma_commit(&dq_full[b]);
@@ -351,10 +367,11 @@ __global__ void __launch_bounds__(512, 1)
         drain_wait(&drain[warp - 1], 0);
       }
     }
-  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
+  } else if ((warp >= 4 && warp < 8) || (warp >= 12 && warp < 16)) {
     // ------------------------------------------------------------ compute: P^T, dS^T
     // Warpgroup h = 0 (warps 4-7) owns query columns [0, CW) of every tile,
-    // h = 1 (warps 12-15) owns [CW, BQ); one key row per thread (TMEM lane).
+    // h = 1 (warps 12-15) owns [CW, BQ); one key row per thread (TMEM lane),
+    // 16 columns at a time.
     constexpr int CW = BQ / 2;
     const int h = warp >= 12 ? 1 : 0;
     const int quarter = warp & 3;
@@ -396,23 +413,23 @@ __global__ void __launch_bounds__(512, 1)
       if (!(ok = warp_wait(sdp_full, it & 1, abort_flag, status))) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int sc = 0; sc < CW / 32; ++sc) {
-        const int col = h * CW + 32 * sc;  // first column of this 32-column sub-chunk
-        float s[32], dp[32];
-        tmem_ld32(lane_base + C::COL_S + col, s);
-        tmem_ld32(lane_base + C::COL_DP + col, dp);
+      for (int sc = 0; sc < CW / 16; ++sc) {
+        const int col = h * CW + 16 * sc;  // first column of this 16-column sub-chunk
+        float s[16], dp[16];
+        tmem_ld16(lane_base + C::COL_S + col, s);
+        tmem_ld16(lane_base + C::COL_DP + col, dp);
         tmem_ld_wait(s);
         tmem_ld_wait(dp);
-        if (sc == CW / 32 - 1) {  // S^T / dP^T columns may now be overwritten by the next tile
+        if (sc == CW / 16 - 1) {  // S^T / dP^T columns may now be overwritten by the next tile
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(sdp_empty);
         }
         const int c0 = q0 + col;  // first query of this sub-chunk
         const bool need_mask = (CAUSAL && c0 < kv0 + C::BKV - 1) || (kv0 + C::BKV > N);
-        uint32_t pp[16], dd[16];
+        uint32_t pp[8], dd[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const int c = 2 * i;
           const float2 nl = *reinterpret_cast<const float2*>(sNL + col + c);
           const float2 nd = *reinterpret_cast<const float2*>(sND + col + c);
@@ -430,19 +447,27 @@ __global__ void __launch_bounds__(512, 1)
           pp[i] = pack2(p0, p1, BF16);
           dd[i] = pack2(d0, d1, BF16);
         }
-        // The buffer is free once the products of the previous tile are done.
+        // The buffers are free once the products of the previous tile are done.
         if (sc == 0 && !(ok = warp_wait(&pds_empty[pb], ((it / C::PS) & 1) ^ 1, abort_flag, status))) break;
-        uint8_t* prow = sP + pb * C::PT_TILE + (col >> 6) * C::PT_SLAB;
+        if (C::PT_TMEM) {
+          tmem_st8(lane_base + C::COL_PT + col / 2, pp);
+          tmem_st8(lane_base + C::COL_DST + col / 2, dd);
+        } else {
+          uint8_t* prow = sP + pb * C::PT_TILE + (col >> 6) * C::PT_SLAB;
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            *reinterpret_cast<uint4*>(prow + sw128_offset(r, (col & 63) + 8 * q)) =
+                make_uint4(pp[4 * q], pp[4 * q + 1], pp[4 * q + 2], pp[4 * q + 3]);
+        }
         uint8_t* drow = sDS + pb * C::PT_TILE + (col >> 6) * C::PT_SLAB;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          *reinterpret_cast<uint4*>(prow + sw128_offset(r, (col & 63) + 8 * q)) =
-              make_uint4(pp[4 * q], pp[4 * q + 1], pp[4 * q + 2], pp[4 * q + 3]);
+        for (int q = 0; q < 2; ++q)
           *reinterpret_cast<uint4*>(drow + sw128_offset(r, (col & 63) + 8 * q)) =
               make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
-        }
       }
       if (!ok) break;
+      if (C::PT_TMEM) tmem_st_wait();
+      tc_fence_before();
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pds_full[pb]);
@@ -455,46 +480,47 @@ __global__ void __launch_bounds__(512, 1)
         store_rows_from_tmem<D, BF16>(lane_base + C::COL_DV, dst, key < N, 1.f);
       }
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else if ((warp >= 8 && warp < 12) || warp >= 16) {
     // ------------------------------------------------------------ dQ drain
+    // Two warpgroups (g = 0: warps 8-11, g = 1: warps 16-19) each add 32 of
+    // the 64 columns of the dQ partial into the float32 accumulator.
+    const int g = warp >= 16 ? 1 : 0;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int b = it & 1;
-      if (!(ok = warp_wait(&dq_full[b], (it >> 1) & 1, abort_flag, status))) break;
+      const int b = it % C::DQB;
+      if (!(ok = warp_wait(&dq_full[b], (it / C::DQB) & 1, abort_flag, status))) break;
       tc_fence_after();
-      float v[2][32];
-      tmem_ld32(lane_base + C::COL_DQ + 64 * b, v[0]);
-      tmem_ld32(lane_base + C::COL_DQ + 64 * b + 32, v[1]);
-      tmem_ld_wait(v[0]);
-      tmem_ld_wait(v[1]);
+      float v[32];
+      tmem_ld32(lane_base + C::COL_DQ + 64 * b + 32 * g, v);
+      tmem_ld_wait(v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&dq_empty[b]);
       const int q0 = (i_begin + it) * BQ;
-      if (C::DQT) {  // lane = feature r, column = query q0 + c: one 128-byte line per warp and column
-        float* base = dq_accum + (head_row + q0) * D + r;
+      if (C::DQT) {  // lane = feature r, column = query q0 + 32g + c: one 128-byte line per warp and column
+        float* base = dq_accum + (head_row + q0 + 32 * g) * D + r;
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (q0 + c < N) red_add_f32(base + (long long)c * D, v[c >> 5][c & 31]);
-      } else {  // lane = query q0 + r, column = feature
+        for (int c = 0; c < 32; ++c)
+          if (q0 + 32 * g + c < N) red_add_f32(base + (long long)c * D, v[c]);
+      } else {  // lane = query q0 + r, column = feature 32g + c
         if (q0 + r < N) {
-          float* base = dq_accum + (head_row + q0 + r) * D;
+          float* base = dq_accum + (head_row + q0 + r) * D + 32 * g;
 #pragma unroll
-          for (int c = 0; c < 64; c += 4)
-            red_add_v4(base + c, v[c >> 5][c & 31], v[c >> 5][(c & 31) + 1], v[c >> 5][(c & 31) + 2],
-                       v[c >> 5][(c & 31) + 3]);
+          for (int c = 0; c < 32; c += 4) red_add_v4(base + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
         }
       }
     }
-    if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
-    if (ok) {
-      tc_fence_after();
-      const int key = kv0 + r;
-      uint4* dst = reinterpret_cast<uint4*>(dk) + (head_row + key) * (D / 8);
-      store_rows_from_tmem<D, BF16>(lane_base + C::COL_DK, dst, key < N, scale);
+    if (g == 0) {
+      if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
+      if (ok) {
+        tc_fence_after();
+        const int key = kv0 + r;
+        uint4* dst = reinterpret_cast<uint4*>(dk) + (head_row + key) * (D / 8);
+        store_rows_from_tmem<D, BF16>(lane_base + C::COL_DK, dst, key < N, scale);
+      }
     }
   }
 
