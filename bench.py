@@ -30,6 +30,10 @@ if ROOT not in sys.path:
 
 METRIC = "attention TFLOPS (fwd, fwd+bwd) & % of GB300 dense BF16 tensor peak, N=4K–32K"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) of one dK/dV launch on C4 from the ncu capture summarised in
+# profiles/fa_bwd_dkdv_C4_causal_n8192_d128_bf16.md.  Must be reset to None whenever that
+# kernel changes until a new capture is taken.
+DKDV_TRAFFIC_C4 = 809710848 + 487737600
 
 
 def load_peaks():
@@ -268,7 +272,8 @@ def run_gpu(args, w, world, rank, local):
                           "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)},
             "roofline": {"bound": "tensor", "kernel": "fa_bwd_dkdv_kernel<128,causal,bf16>",
                          "achieved": round(dkdv_tflops, 1), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(dkdv_tflops / peak, 4), "traffic": None,
+                         "frac": round(dkdv_tflops / peak, 4),
+                         "traffic": DKDV_TRAFFIC_C4 if w.name.startswith("C4") else None,
                          "peak_source": f"{peak_src} bf16_tflops (burst)",
                          "algorithmic": "10*N^2*d per head (5 GEMMs), halved causal, per launch"},
             "peak_memory_bytes": int(peak_mem), "inputs_bytes": int(mem_inputs),
