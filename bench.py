@@ -30,9 +30,9 @@ if ROOT not in sys.path:
 
 METRIC = "attention TFLOPS (fwd, fwd+bwd) & % of GB300 dense BF16 tensor peak, N=4K–32K"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) of one dK/dV launch on C4 from the ncu capture summarised in
-# profiles/fa_bwd_dkdv_C4_causal_n8192_d128_bf16.md.  Must be reset to None whenever that
-# kernel changes until a new capture is taken.
+# DRAM bytes (read + write) of one dK/dV launch on C4, from an ncu capture of the current
+# kernel (dram__bytes_read.sum + dram__bytes_write.sum).  Reset to None whenever that kernel
+# changes, until a new capture is taken.
 DKDV_TRAFFIC_C4 = 809710848 + 487737600
 
 
