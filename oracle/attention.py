@@ -8,8 +8,10 @@ Definitions followed
   section 3.1 (safe softmax: subtract the row max, exponentiate, divide by
   the row sum).  The scale ``s`` is a parameter; the pages use 1/sqrt(d).
 * Causal mask: P3 section 3.2 (masked scores are set to -inf so they add
-  nothing to m, l or O); key j is visible to query i iff j <= i (top-left
-  alignment, square problem).
+  nothing to m, l or O); key j is visible to query i iff j <= i (square
+  problem).  With Nq queries and Nk >= Nq keys (decoding) the queries are
+  read as the last Nq positions: key j is visible to query i iff
+  j <= i + Nk - Nq, which is the square rule when Nq = Nk.
 * LSE: P3 section 3.2, natural log: LSE_i = m_i + log(l_i) with m_i the row
   max of the *scaled* scores.
 * Backward: P3 section 3.3 -- with G = dO and A = G V^T,
@@ -31,7 +33,8 @@ import numpy as np
 def _scores(q, k, scale, causal, rows=None):
     """S = s * Q K^T for the query rows ``rows`` (all rows if None).
 
-    Causal: entries with key index > query index become -inf (P3 section 3.2).
+    Causal: entries with key index > query position become -inf (P3 section
+    3.2); query i sits at position i + Nk - Nq.
     """
     if rows is None:
         rows = np.arange(q.shape[0])
@@ -39,7 +42,8 @@ def _scores(q, k, scale, causal, rows=None):
     s = scale * (q[rows] @ k.T)
     if causal:
         keys = np.arange(k.shape[0])
-        s = np.where(keys[None, :] > rows[:, None], -np.inf, s)
+        pos = rows + (k.shape[0] - q.shape[0])
+        s = np.where(keys[None, :] > pos[:, None], -np.inf, s)
     return s
 
 

@@ -15,7 +15,8 @@ with block max m_blk:
 
 starting from m = -inf, l = 0, O = 0 with the factor exp(m - m') taken as 0
 while m is still -inf.  The result is O / l and the LSE is m + log l.
-Masked (causal) scores are -inf and contribute nothing (same section).
+Masked (causal) scores are -inf and contribute nothing (same section); with
+fewer queries than keys the queries are the last positions.
 
 Here all query rows advance together and keys stream in blocks of
 ``block`` rows (1 = one key at a time, the Milakov-Gimelshein online
@@ -43,7 +44,7 @@ def online_attention(q, k, v, block, scale=None, causal=False, trace_row=None,
     l = np.zeros(n_q)
     acc = np.zeros((n_q, v.shape[1]))
     trace = []
-    query_idx = np.arange(n_q)
+    query_idx = np.arange(n_q) + (n_k - n_q)  # query positions (last n_q of n_k)
     for j0 in range(0, n_k, block):
         j1 = min(n_k, j0 + block)
         s = scale * (q @ k[j0:j1].T)                      # [n_q, blk]

@@ -270,3 +270,48 @@ def test_planted_mistakes_are_caught(name, monkeypatch):
     monkeypatch.setitem(A.__dict__, "_orig_scores", A._scores)
     monkeypatch.setattr(A, attr, bad)
     assert not _pins_pass(), f"pin missed: {name}"
+
+
+# ------------------------------------------------ fewer queries than keys
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (1, 37), (5, 37), (16, 300)])
+def test_rectangular_against_torch(causal, Nq, Nk):
+    """Nq <= Nk: torch float64 SDPA with an explicit mask (queries are the last
+    Nq positions, so query i sees keys j <= i + Nk - Nq)."""
+    rng = np.random.default_rng(Nq * 1000 + Nk)
+    d, s = 16, 0.3
+    q = rng.normal(size=(Nq, d))
+    k, v, = rng.normal(size=(Nk, d)), rng.normal(size=(Nk, d))
+    o, lse = A.forward_head(q, k, v, s, causal)
+    mask = None
+    if causal:
+        mask = torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+    to = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q)[None], torch.tensor(k)[None], torch.tensor(v)[None], attn_mask=mask, scale=s)[0]
+    assert np.abs(o - to.numpy()).max() < 1e-12
+    full = s * q @ k.T
+    if causal:
+        full = np.where(mask.numpy(), full, -np.inf)
+    assert np.allclose(lse, scipy.special.logsumexp(full, axis=1), atol=1e-13)
+    # The last query sees every key: the mask does not change its row.
+    o_nc, _ = A.forward_head(q, k, v, s, False)
+    assert np.abs(o[-1] - o_nc[-1]).max() < 1e-14
+    # The streamed recurrence agrees for any key block size.
+    for block in (1, 7, 64):
+        so, slse, _ = OL.online_attention(q, k, v, block, scale=s, causal=causal)
+        assert np.abs(so - o).max() < 2e-15 and np.abs(slse - lse).max() < 1e-13
+
+
+def test_key_splits_combine_by_lse():
+    """Attention over a key range split in parts equals the LSE-weighted
+    combination of the parts: O = sum_s exp(LSE_s - LSE) O_s, LSE = log sum_s exp(LSE_s)."""
+    rng = np.random.default_rng(3)
+    Nq, Nk, d, s = 4, 1000, 32, 0.2
+    q, k, v = rng.normal(size=(Nq, d)), rng.normal(size=(Nk, d)), rng.normal(size=(Nk, d))
+    o, lse = A.forward_head(q, k, v, s, False)
+    parts = [(0, 130), (130, 131), (131, 600), (600, 1000)]
+    lses = np.stack([A.forward_head(q, k[a:b], v[a:b], s, False)[1] for a, b in parts])
+    outs = np.stack([A.forward_head(q, k[a:b], v[a:b], s, False)[0] for a, b in parts])
+    comb_lse = scipy.special.logsumexp(lses, axis=0)
+    comb_o = (np.exp(lses - comb_lse)[:, :, None] * outs).sum(axis=0)
+    assert np.abs(comb_lse - lse).max() < 1e-13 and np.abs(comb_o - o).max() < 1e-14
