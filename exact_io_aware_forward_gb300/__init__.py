@@ -6,6 +6,6 @@ Importing this package does not load the library; the first call does, and
 fails loudly if it has not been built.
 """
 from .api import (FAError, backward, fa_backward, fa_backward_dkdv, fa_backward_dq_convert,  # noqa: F401
-                  fa_backward_noalloc,
+                  fa_backward_noalloc, fa_decode_workspace_size, fa_forward_decode, forward_decode,
                   fa_backward_preprocess, fa_backward_workspace_size, fa_device_status, fa_forward,
                   forward)

@@ -135,6 +135,26 @@ def fa_backward_dq_convert(dq_accum, dq, scale=None, stream=None) -> None:
                                                                   _scale(scale, d), _stream(stream)))
 
 
+def fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits=0) -> int:
+    return int(lib().fa_decode_workspace_size(B, H, Nq, Nk, d, num_splits))
+
+
+def fa_forward_decode(q, k, v, o, lse, workspace, causal=False, scale=None, num_splits=0, stream=None) -> None:
+    """Split-KV forward: q, o [B,H,Nq,d]; k, v [B,H,Nk,d]; lse [B,H,Nq]."""
+    B, H, Nq, d = _shape(q)
+    dt = q.dtype
+    if k.dim() != 4 or k.shape[:2] != q.shape[:2] or k.shape[3] != d:
+        raise ValueError("k must be [B, H, Nk, d] with q's B, H, d")
+    Nk = k.shape[2]
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    args = [_bhnd("q", q), _bhnd("k", k, None, dt), _bhnd("v", v, k.shape, dt), _bhnd("o", o, q.shape, dt),
+            _bhnd("lse", lse, (B, H, Nq), torch.float32)]
+    _check("fa_forward_decode", lib().fa_forward_decode(*args, B, H, Nq, Nk, d, _DTYPE_CODE[dt], int(bool(causal)),
+                                                        _scale(scale, d), int(num_splits), workspace.data_ptr(),
+                                                        workspace.numel(), _stream(stream)))
+
+
 def fa_device_status(stream=None) -> None:
     """Synchronise ``stream``; raise FAError if a kernel latched a timeout."""
     _check("fa_device_status", lib().fa_device_status(_stream(stream)))
@@ -147,6 +167,18 @@ def forward(q, k, v, causal=False, scale=None, stream=None):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     fa_forward(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def forward_decode(q, k, v, causal=False, scale=None, num_splits=0, stream=None, workspace=None):
+    """Return (O, LSE) for few queries q [B,H,Nq,d] against k, v [B,H,Nk,d]."""
+    B, H, Nq, d = _shape(q)
+    if workspace is None:
+        n = fa_decode_workspace_size(B, H, Nq, k.shape[2], d, num_splits)
+        workspace = torch.empty(max(n, 1), device=q.device, dtype=torch.uint8)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    fa_forward_decode(q, k, v, o, lse, workspace, causal, scale, num_splits, stream)
     return o, lse
 
 

@@ -192,6 +192,66 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   return fa_backward_dq_convert(dq_accum, dq, B, H, N, d, dtype, scale, stream);
 }
 
+namespace {
+fa_status decode_plan(int B, int H, int Nq, int Nk, int d, int num_splits, int* splits, int* chunk,
+                      size_t* bytes) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH > 65535 || BH * Nk * d >= (1LL << 31) || BH * Nq * d >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  if (num_splits < 0 || num_splits > 1024) return FA_ERR_INVALID_ARG;
+  int s = num_splits ? num_splits : fa::decode_default_splits((int)BH, Nq, Nk);
+  const int c = fa::decode_chunk(Nk, s);
+  s = (Nk + c - 1) / c;  // no empty trailing chunk
+  const size_t rows = (size_t)s * BH * Nq;
+  *splits = s;
+  *chunk = c;
+  *bytes = align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+  return FA_OK;
+}
+}  // namespace
+
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  int s, c;
+  size_t bytes = 0;
+  return decode_plan(B, H, Nq, Nk, d, num_splits, &s, &c, &bytes) == FA_OK ? bytes : 0;
+}
+
+fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                            int Nq, int Nk, int d, int dtype, int causal, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  int splits, chunk;
+  size_t need;
+  fa_status st = decode_plan(B, H, Nq, Nk, d, num_splits, &splits, &chunk, &need);
+  if (st != FA_OK) return st;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  fa::DecodeArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.BH = B * H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.num_splits = splits;
+  a.chunk = chunk;
+  a.causal = causal != 0;
+  a.scale_log2 = scale * kLog2e;
+  const size_t rows = (size_t)splits * a.BH * Nq;
+  a.o_part = static_cast<float*>(workspace);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)));
+  if (fa::launch_decode(d, dtype == FA_BF16, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 fa_status fa_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   unsigned int v = 0;

@@ -43,4 +43,22 @@ cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const vo
 cudaError_t launch_backward_dq_convert(int d, bool bf16, const float* dq_accum, void* dq, long long rows,
                                        float scale, cudaStream_t stream);
 
+struct DecodeArgs {
+  const void* q;       // [B*H, Nq, d]
+  const void* k;       // [B*H, Nk, d]
+  const void* v;       // [B*H, Nk, d]
+  void* o;             // [B*H, Nq, d]
+  float* lse;          // [B*H, Nq]
+  float* o_part;       // [num_splits, B*H, Nq, d] float32
+  float* lse_part;     // [num_splits, B*H, Nq] float32, log2 units
+  int BH, Nq, Nk;
+  int num_splits;
+  int chunk;           // keys per split (multiple of 256)
+  bool causal;
+  float scale_log2;
+};
+int decode_default_splits(int BH, int Nq, int Nk);
+int decode_chunk(int Nk, int num_splits);
+cudaError_t launch_decode(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream);
+
 }  // namespace fa

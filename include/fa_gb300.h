@@ -119,6 +119,26 @@ fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, 
                                  float scale, void* stream);
 
 /*
+ * Split-KV forward for few queries against many keys (decoding).
+ * q, o: [B,H,Nq,d]; k, v: [B,H,Nk,d]; lse: [B,H,Nq] float32 (natural log, as
+ * fa_forward).  Same result as fa_forward on a rectangular problem: the key
+ * range of every head is cut into `num_splits` chunks, each chunk yields its
+ * normalised output and log-sum-exp with the online-softmax recurrence
+ * (tutorial section 3.2), and the chunks are merged exactly by
+ * LSE = log sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
+ * Causal: the queries are the last Nq of the Nk positions, so key j is
+ * visible to query i iff j <= i + Nk - Nq (requires Nq <= Nk).
+ * num_splits = 0 picks a count that fills the GPU; otherwise 1..1024.
+ * workspace: fa_decode_workspace_size(B,H,Nq,Nk,d,num_splits) bytes of
+ * device memory (partial outputs), contents irrelevant on entry.
+ * Supported: d in {64, 128}, fp16/bf16, B*H <= 65535, Nq, Nk >= 1.
+ */
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                            int Nq, int Nk, int d, int dtype, int causal, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Size of the fixed device scratch array used by fa_backward_noalloc.
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

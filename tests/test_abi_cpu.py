@@ -82,3 +82,16 @@ def test_backward_rejects_small_workspace(lib):
     rc = lib.fa_backward(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125,
                          ptr, 16, None)
     assert rc == 5
+
+
+def test_decode_workspace_and_validation(lib):
+    ws = lib.fa_decode_workspace_size
+    assert ws(1, 1, 1, 0, 128, 0) == 0 and ws(1, 1, 1, 100, 96, 0) == 0 and ws(1, 1, 1, 100, 128, 2000) == 0
+    n = ws(1, 2, 3, 1000, 64, 4)  # 4 chunks of 256 keys, 6 rows each
+    assert n == ((4 * 6 * 64 * 4 + 255) // 256) * 256 + ((4 * 6 * 4 + 255) // 256) * 256
+    ptr = 1 << 20
+    # causal with more queries than keys has no reading: rejected before any launch
+    rc = lib.fa_forward_decode(ptr, ptr, ptr, ptr, ptr, 1, 1, 8, 4, 64, 1, 1, 0.125, 0, ptr, 1 << 20, None)
+    assert rc == 1
+    rc = lib.fa_forward_decode(ptr, ptr, ptr, ptr, ptr, 1, 1, 2, 4, 64, 1, 0, 0.125, 0, ptr, 16, None)
+    assert rc == 5
