@@ -144,6 +144,112 @@ def oracle_sample(w, budget_s: float, max_heads: int):
     return per_head * heads / spent / 1e12, heads, spent, threads
 
 
+# ---------------------------------------------------------------- decode (split-KV)
+def oracle_decode_sample(w, budget_s: float, max_heads: int):
+    """float64 oracle on whole heads of a decode workload; GB/s of K/V covered."""
+    from exact_io_aware_forward_gb300.synth import as_float64, attention_inputs
+    from oracle import attention as A
+    heads, spent = 0, 0.0
+    scale = 1.0 / math.sqrt(w.d)
+    wall0 = time.perf_counter()  # the budget also covers input generation
+    while heads < min(max_heads, w.B * w.H) and (heads == 0 or time.perf_counter() - wall0 < budget_s):
+        q, _, _, _ = attention_inputs(1, 1, w.Nq, w.d, w.dtype, seed=w.seed * 1000 + heads, with_do=False)
+        _, k, v, _ = attention_inputs(1, 1, w.Nk, w.d, w.dtype, seed=w.seed * 1000 + heads + 1, with_do=False)
+        q, k, v = as_float64(q, k, v)
+        t0 = time.perf_counter()
+        A.forward_head(q[0, 0], k[0, 0], v[0, 0], scale, w.causal)
+        spent += time.perf_counter() - t0
+        heads += 1
+    per_head = w.kv_bytes() / (w.B * w.H)
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return per_head * heads / spent / 1e9, heads, spent, threads
+
+
+def measure_decode(dev, w, steps, warmup):
+    """Device-resident timing of fa_forward_decode (split + combine kernels) on
+    workload `w`; the L2 is flushed before every timed call."""
+    import torch
+
+    import exact_io_aware_forward_gb300 as fa
+    from exact_io_aware_forward_gb300.synth import decode_inputs
+
+    q, k, v = (x.to(dev) for x in decode_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), device=dev, dtype=torch.float32)
+    ws = torch.empty(fa.fa_decode_workspace_size(w.B, w.H, w.Nq, w.Nk, w.d, 0), device=dev, dtype=torch.uint8)
+    flush = torch.empty(256 << 20, device=dev, dtype=torch.uint8)
+    for _ in range(warmup):
+        fa.fa_forward_decode(q, k, v, o, lse, ws, w.causal)
+    fa.fa_device_status()
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fa.fa_forward_decode(q, k, v, o, lse, ws, w.causal)
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    fa.fa_device_status()
+    ms = total / steps
+    byts = w.kv_bytes() + 2 * (w.B * w.H * w.Nq * w.d * 2)
+    return ms, byts, (q, k, v, ws)
+
+
+def run_decode(args, world, rank, local):
+    import torch
+
+    import exact_io_aware_forward_gb300 as fa
+    from exact_io_aware_forward_gb300.synth import D1 as w
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms, byts, (q, k, v, ws) = measure_decode(dev, w, args.steps, args.warmup)
+    clocks = sampler.stop()
+    gbs = byts / (ms * 1e-3) / 1e9
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    ho = torch.empty_like(hq).pin_memory()
+    hl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        gq, gk, gv = (x.to(dev, non_blocking=True) for x in (hq, hk, hv))
+        go, gl = fa.forward_decode(gq, gk, gv, causal=w.causal, workspace=ws)
+        ho.copy_(go, non_blocking=True)
+        hl.copy_(gl, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    c0 = time.perf_counter()
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - c0) * 1e3 / 3
+    cpu, heads, spent, threads = oracle_decode_sample(w, args.cpu_budget, 4096)
+    peak = float(peaks["hbm_gbs"])
+    return {
+        "metric": "split-KV decode throughput (K/V bytes streamed per second)", "value": round(world * gbs, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) Q, K, V; no dataset)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+                   "l2": "flushed (256 MB write) before every timed call"},
+        "roofline": {"bound": "hbm", "kernel": "fa_decode_split_kernel + fa_decode_combine_kernel",
+                     "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                     "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
+                     "algorithmic": "K + V + Q + O bytes per call"},
+        "e2e": {"value": round(world * byts / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
+                "d2h_bytes_per_step": int(ho.numel() * 2 + hl.numel() * 4), "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": {"value": cpu, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{heads} whole head(s) of {w.name}, float64 forward, {spent:.1f} s"},
+    }
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_gpu(args, w, world, rank, local):
     import torch
@@ -284,6 +390,12 @@ def run_gpu(args, w, world, rank, local):
             "gpu_launches": 4 * args.steps,
             "clocks": clocks,
         }
+    if rank == 0:
+        from exact_io_aware_forward_gb300.synth import D1
+        dms, dbytes, _ = measure_decode(dev, D1, 10, 3)
+        dgbs = dbytes / (dms * 1e-3) / 1e9
+        result["decode"] = {"workload": D1.name, "ms": round(dms, 4), "GB_per_s": round(dgbs, 1),
+                            "frac_of_hbm_peak": round(dgbs / float(peaks["hbm_gbs"]), 4)}
     if dist:
         dist.destroy_process_group()
     return result
@@ -322,6 +434,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="C4", help="C2, C3N, C3C, C4 or C5")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", default="train", choices=["train", "decode"],
+                    help="train: fwd+bwd step (the headline); decode: split-KV decoding line")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing (rank 0, N=1)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -329,6 +443,13 @@ def main():
     from exact_io_aware_forward_gb300.synth import WORKLOADS
     w = WORKLOADS[args.workload]
     world, rank, local = dist_env()
+    if args.impl == "ours" and args.mode == "decode":
+        from exact_io_aware_forward_gb300 import build as fa_build
+        fa_build.build()
+        out = run_decode(args, world, rank, local)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
     if args.impl == "reference":
         out = run_reference(args, w, world, rank)
     else:

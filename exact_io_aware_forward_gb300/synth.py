@@ -93,6 +93,35 @@ def workload_inputs(w: Workload, with_do: bool | None = None):
     return attention_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.k_row_scale, with_do)
 
 
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """Few queries (the last Nq positions) against Nk keys per head."""
+
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    dtype: str
+    causal: bool
+    seed: int
+
+    def kv_bytes(self) -> int:
+        return 2 * self.B * self.H * self.Nk * self.d * 2
+
+
+# Decoding workload at the long end of the specified sequence range.
+D1 = DecodeWorkload("D1 decode causal Nq=1 Nk=32768 d=128 bf16", 4, 32, 1, 32768, 128, "bf16", True, 6)
+
+
+def decode_inputs(w: DecodeWorkload):
+    """(q [B,H,Nq,d], k, v [B,H,Nk,d]) drawn like ``attention_inputs``."""
+    q, _, _, _ = attention_inputs(w.B, w.H, w.Nq, w.d, w.dtype, seed=w.seed, with_do=False)
+    _, k, v, _ = attention_inputs(w.B, w.H, w.Nk, w.d, w.dtype, seed=w.seed + 1, with_do=False)
+    return q, k, v
+
+
 def page_inputs(N: int, D: int, seed: int):
     """float64 Q, K, V of one head, drawn like the tutorial page's demos."""
     rng = np.random.default_rng(seed)

@@ -70,8 +70,8 @@ def test_decode_square_equals_forward():
 
 def test_decode_full_size_sampled_heads():
     """Decode workload D1: B=4, H=32, one query, Nk=32768, d=128, bf16, causal."""
-    B, H, Nq, Nk, d = 4, 32, 1, 32768, 128
-    q, k, v = _inputs(B, H, Nq, Nk, d, "bf16", seed=5)
+    from exact_io_aware_forward_gb300.synth import D1, decode_inputs
+    q, k, v = decode_inputs(D1)
     dev = torch.device("cuda:0")
     o, lse = fa.forward_decode(q.to(dev), k.to(dev), v.to(dev), causal=True)
     fa.fa_device_status()
