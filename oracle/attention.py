@@ -19,6 +19,12 @@ Definitions followed
   The row sum is taken over A * P exactly as written there, not through the
   rowsum(dO * O) shortcut the CUDA path uses.
 
+* Block-sparse attention (P3 section 06: the whole-block skip generalised to
+  any sparsity pattern): a boolean block mask over 128 x 128 (query, key)
+  blocks removes whole blocks, i.e. their scores are -inf like masked causal
+  scores.  A query row with no visible key at all has no softmax; the
+  reading taken is O = 0 and LSE = -inf for it (and no gradient flows).
+
 Arrays are numpy float64.  Batched entry points take [B, H, N, d] arrays and
 loop over heads; the ``*_head`` functions take one head [N, d].
 """
@@ -30,11 +36,15 @@ import numpy as np
 # --------------------------------------------------------------------------
 # building blocks (kept separate so that tests can plant mistakes in them)
 # --------------------------------------------------------------------------
-def _scores(q, k, scale, causal, rows=None):
+BLOCK = 128  # rows / columns of one block of a block mask
+
+
+def _scores(q, k, scale, causal, rows=None, block_mask=None):
     """S = s * Q K^T for the query rows ``rows`` (all rows if None).
 
     Causal: entries with key index > query position become -inf (P3 section
-    3.2); query i sits at position i + Nk - Nq.
+    3.2); query i sits at position i + Nk - Nq.  ``block_mask`` (boolean,
+    [ceil(Nq/128), ceil(Nk/128)]): entries of blocks marked False become -inf.
     """
     if rows is None:
         rows = np.arange(q.shape[0])
@@ -44,18 +54,24 @@ def _scores(q, k, scale, causal, rows=None):
         keys = np.arange(k.shape[0])
         pos = rows + (k.shape[0] - q.shape[0])
         s = np.where(keys[None, :] > pos[:, None], -np.inf, s)
+    if block_mask is not None:
+        bm = np.asarray(block_mask, dtype=bool)
+        keep = bm[rows // BLOCK][:, np.arange(k.shape[0]) // BLOCK]
+        s = np.where(keep, s, -np.inf)
     return s
 
 
 def _softmax_rows(s):
     """Safe softmax of every row (P3 section 3.1).
 
-    Returns (P, m, l) with m the row max and l = sum exp(s - m).
+    Returns (P, m, l) with m the row max and l = sum exp(s - m).  A row whose
+    scores are all -inf (no visible key) gets P = 0, m = -inf, l = 0.
     """
     m = s.max(axis=1)
-    e = np.exp(s - m[:, None])
+    empty = np.isneginf(m)
+    e = np.exp(s - np.where(empty, 0.0, m)[:, None])
     l = e.sum(axis=1)
-    return e / l[:, None], m, l
+    return e / np.where(empty, 1.0, l)[:, None], m, l
 
 
 def _softmax_backward(p, a):
@@ -66,11 +82,12 @@ def _softmax_backward(p, a):
 # --------------------------------------------------------------------------
 # one head
 # --------------------------------------------------------------------------
-def forward_head(q, k, v, scale, causal=False, rows=None):
+def forward_head(q, k, v, scale, causal=False, rows=None, block_mask=None):
     """O and LSE of one head ([N, d] inputs) for the query rows ``rows``."""
-    s = _scores(q, k, scale, causal, rows)
+    s = _scores(q, k, scale, causal, rows, block_mask)
     p, m, l = _softmax_rows(s)
-    return p @ v, m + np.log(l)
+    with np.errstate(divide="ignore"):
+        return p @ v, m + np.log(l)
 
 
 def probabilities_head(q, k, scale, causal=False, rows=None):
@@ -79,9 +96,9 @@ def probabilities_head(q, k, scale, causal=False, rows=None):
     return p
 
 
-def backward_head(q, k, v, do, scale, causal=False):
+def backward_head(q, k, v, do, scale, causal=False, block_mask=None):
     """(dQ, dK, dV) of one head, everything materialised (P3 section 3.3)."""
-    p, _, _ = _softmax_rows(_scores(q, k, scale, causal))
+    p, _, _ = _softmax_rows(_scores(q, k, scale, causal, block_mask=block_mask))
     a = do @ v.T
     ds = _softmax_backward(p, a)
     dq = scale * (ds @ k)

@@ -245,9 +245,10 @@ MUTANTS = {
     "row sum over the wrong axis":
         ("_softmax_backward", lambda p, a: p * (a - (a * p).sum(axis=0, keepdims=True))),
     "scores without the scale":
-        ("_scores", lambda q, k, scale, causal, rows=None: A.__dict__["_orig_scores"](q, k, 1.0, causal, rows)),
+        ("_scores", lambda q, k, scale, causal, rows=None, block_mask=None:
+         A.__dict__["_orig_scores"](q, k, 1.0, causal, rows, block_mask)),
     "causal mask shifted by one":
-        ("_scores", lambda q, k, scale, causal, rows=None: _shifted_mask(q, k, scale, causal, rows)),
+        ("_scores", lambda q, k, scale, causal, rows=None, block_mask=None: _shifted_mask(q, k, scale, causal, rows)),
     "softmax without the normalisation":
         ("_softmax_rows", lambda s: (np.exp(s - s.max(axis=1)[:, None]), s.max(axis=1), np.ones(s.shape[0]))),
 }
@@ -315,3 +316,77 @@ def test_key_splits_combine_by_lse():
     comb_lse = scipy.special.logsumexp(lses, axis=0)
     comb_o = (np.exp(lses - comb_lse)[:, :, None] * outs).sum(axis=0)
     assert np.abs(comb_lse - lse).max() < 1e-13 and np.abs(comb_o - o).max() < 1e-14
+
+
+# ------------------------------------------------ block-sparse masks
+def _random_block_mask(Tq, Tk, rng, density=0.5, full_rows=True):
+    bm = rng.random((Tq, Tk)) < density
+    if full_rows:  # every query block keeps at least one key block
+        bm[np.arange(Tq), rng.integers(0, Tk, Tq)] = True
+    return bm
+
+
+def test_block_mask_all_ones_is_dense_and_causal_pattern_is_causal():
+    rng = np.random.default_rng(21)
+    N, d, s = 300, 8, 0.4
+    q, k, v, do = (rng.normal(size=(N, d)) for _ in range(4))
+    T = (N + 127) // 128
+    ones = np.ones((T, T), bool)
+    for causal in (False, True):
+        o1, l1 = A.forward_head(q, k, v, s, causal)
+        o2, l2 = A.forward_head(q, k, v, s, causal, block_mask=ones)
+        assert np.abs(o1 - o2).max() == 0 and np.abs(l1 - l2).max() == 0
+    tri = np.tril(ones)  # blocks above the diagonal are fully masked by causality anyway
+    o1, l1 = A.forward_head(q, k, v, s, True)
+    o2, l2 = A.forward_head(q, k, v, s, True, block_mask=tri)
+    assert np.abs(o1 - o2).max() == 0
+    g1 = A.backward_head(q, k, v, do, s, True)
+    g2 = A.backward_head(q, k, v, do, s, True, block_mask=tri)
+    assert all(np.abs(a - b).max() == 0 for a, b in zip(g1, g2))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_against_torch(causal):
+    """Random block masks = torch float64 SDPA + autograd with the expanded element mask."""
+    rng = np.random.default_rng(22 + causal)
+    N, d, s = 400, 16, 0.3
+    T = (N + 127) // 128
+    bm = _random_block_mask(T, T, rng)
+    if causal:
+        bm[np.arange(T), np.arange(T)] = True  # every row keeps its diagonal block
+    q, k, v, do = (rng.normal(size=(N, d)) for _ in range(4))
+    o, lse = A.forward_head(q, k, v, s, causal, block_mask=bm)
+    dq, dk, dv = A.backward_head(q, k, v, do, s, causal, block_mask=bm)
+    elem = np.kron(bm, np.ones((128, 128), bool))[:N, :N]
+    if causal:
+        elem &= np.tril(np.ones((N, N), bool))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.tensor(elem), scale=s)
+    to.backward(torch.tensor(do))
+    assert np.abs(o - to.detach().numpy()).max() < 1e-12
+    for g, t in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        assert np.abs(g - t.numpy()).max() < 1e-11
+    full = np.where(elem, s * q @ k.T, -np.inf)
+    assert np.allclose(lse, scipy.special.logsumexp(full, axis=1), atol=1e-12)
+    # Streaming only over the kept key blocks gives the same rows (P3 section 3.2 for any block order).
+    for qb in range(T):
+        rows = np.arange(qb * 128, min(N, qb * 128 + 128))
+        keys = np.concatenate([np.arange(kb * 128, min(N, kb * 128 + 128)) for kb in range(T) if bm[qb, kb]])
+        ref_o, ref_l = A.forward_head(q, k, v, s, causal, rows=rows, block_mask=bm)
+        if not causal:
+            so, sl, _ = OL.online_attention(q[rows], k[keys], v[keys], 64, scale=s)
+            assert np.abs(so - ref_o).max() < 2e-15 and np.abs(sl - ref_l).max() < 1e-13
+
+
+def test_rows_without_visible_keys():
+    """Reading for an empty softmax: O = 0, LSE = -inf, and no gradient."""
+    rng = np.random.default_rng(23)
+    N, d, s = 260, 8, 0.5
+    q, k, v, do = (rng.normal(size=(N, d)) for _ in range(4))
+    bm = np.array([[True, False, True], [False, False, False], [False, True, True]])
+    o, lse = A.forward_head(q, k, v, s, False, block_mask=bm)
+    assert np.all(o[128:256] == 0) and np.all(np.isneginf(lse[128:256]))
+    assert np.all(np.isfinite(lse[:128])) and np.all(np.isfinite(lse[256:]))
+    dq, dk, dv = A.backward_head(q, k, v, do, s, False, block_mask=bm)
+    assert np.all(dq[128:256] == 0)
+    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
