@@ -250,6 +250,165 @@ def run_decode(args, world, rank, local):
     }
 
 
+# ---------------------------------------------------------------- block-sparse
+def block_mask_flops(w, bm) -> float:
+    """Forward FLOPs over the kept blocks: 4 * d per (query, key) pair that a
+    kept block covers (2 for Q K^T, 2 for P V), counting only rows and keys that
+    exist in a ragged last tile and, under the causal mask, only key <= query."""
+    import numpy as np
+    T = w.tiles
+    size = np.minimum(128, w.N - 128 * np.arange(T)).astype(np.float64)
+    pairs = np.outer(size, size)
+    if w.causal:
+        pairs = np.tril(pairs)
+        pairs[np.arange(T), np.arange(T)] = size * (size + 1) / 2
+    per_mask = (bm * pairs).sum(axis=(1, 2))
+    total = per_mask.sum() * (w.B * w.H if bm.shape[0] == 1 else 1)
+    return 4.0 * w.d * float(total)
+
+
+def oracle_blocksparse_sample(w, bm, budget_s: float, max_heads: int):
+    """float64 oracle (forward + explicit backward under the block mask) on
+    whole heads until `budget_s` is spent; TFLOP/s in the 2.5 F convention."""
+    from exact_io_aware_forward_gb300.synth import as_float64, attention_inputs
+    from oracle import attention as A
+    heads, spent, flops = 0, 0.0, 0.0
+    scale = 1.0 / math.sqrt(w.d)
+    per_head = block_mask_flops(w, bm) / (w.B * w.H)  # average over heads
+    while heads < max_heads and (heads == 0 or spent < budget_s):
+        q, k, v, do = as_float64(*attention_inputs(1, 1, w.N, w.d, w.dtype, seed=w.seed * 1000 + heads))
+        m = bm[0 if bm.shape[0] == 1 else heads % bm.shape[0]]
+        t0 = time.perf_counter()
+        A.forward_head(q[0, 0], k[0, 0], v[0, 0], scale, w.causal, block_mask=m)
+        A.backward_head(q[0, 0], k[0, 0], v[0, 0], do[0, 0], scale, w.causal, block_mask=m)
+        spent += time.perf_counter() - t0
+        flops += 2.5 * per_head
+        heads += 1
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return flops / spent / 1e12, heads, spent, threads
+
+
+def measure_blocksparse(dev, w, steps, warmup, sampler=None):
+    """Device-resident fwd+bwd under the block mask, each of the four kernels
+    timed with CUDA events on the launching stream."""
+    import torch
+
+    import exact_io_aware_forward_gb300 as fa
+    from exact_io_aware_forward_gb300.synth import blocksparse_inputs
+
+    q, k, v, do, bm = blocksparse_inputs(w)
+    q, k, v, do = (x.to(dev) for x in (q, k, v, do))
+    md = torch.from_numpy(bm.astype("uint8")).to(dev)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.fa_backward_workspace_size(B, H, N, d), device=dev, dtype=torch.uint8)
+    rows = B * H * N
+    delta = ws[: rows * 4].view(torch.float32).view(B, H, N)
+    off = (rows * 4 + 255) // 256 * 256
+    acc = ws[off: off + rows * d * 4].view(torch.float32).view(B, H, N, d)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+
+    def step(e=None):
+        if e: e[0].record(stream)
+        fa.fa_forward_blocksparse(q, k, v, o, lse, md, w.causal)
+        if e: e[1].record(stream)
+        fa.fa_backward_preprocess(o, do, delta, acc)
+        if e: e[2].record(stream)
+        fa.fa_backward_dkdv_blocksparse(q, k, v, do, lse, delta, acc, dk, dv, md, w.causal)
+        if e: e[3].record(stream)
+        fa.fa_backward_dq_convert(acc, dq)
+        if e: e[4].record(stream)
+
+    for _ in range(warmup):
+        step()
+    fa.fa_device_status()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    fa.fa_device_status()
+    parts = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps for j in range(4)]
+    return t0.elapsed_time(t1) / steps, parts, clocks, (q, k, v, do, md, ws, bm)
+
+
+def run_blocksparse(args, world, rank, local):
+    import torch
+
+    import exact_io_aware_forward_gb300 as fa
+    from exact_io_aware_forward_gb300.synth import S1 as w
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    ms, parts, clocks, (q, k, v, do, md, ws, bm) = measure_blocksparse(dev, w, args.steps, args.warmup,
+                                                                         ClockSampler(local))
+    F = block_mask_flops(w, bm)
+    value = 2.5 * F / (ms * 1e-3) / 1e12
+    hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+    hm = md.cpu().pin_memory()
+    ho, hdq, hdk, hdv = (torch.empty_like(x, device="cpu").pin_memory() for x in (q, q, q, q))
+    hlse = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        gq, gk, gv, gdo, gm = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, hdo, hm))
+        go, glse = fa.forward(gq, gk, gv, causal=w.causal, block_mask=gm)
+        gdq, gdk, gdv = fa.backward(gq, gk, gv, go, glse, gdo, causal=w.causal, workspace=ws, block_mask=gm)
+        for h, g in ((ho, go), (hlse, glse), (hdq, gdq), (hdk, gdk), (hdv, gdv)):
+            h.copy_(g, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 10))
+    c0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - c0) * 1e3 / n_e2e
+    fa.fa_device_status()
+    elem = q.numel() * 2
+    peak = float(peaks["bf16_tflops"])
+    dkdv = 2.5 * F / (parts[2] * 1e-3) / 1e12
+    fwd = F / (parts[0] * 1e-3) / 1e12
+    cpu, heads, spent, threads = oracle_blocksparse_sample(w, bm, args.cpu_budget, 64)
+    return {
+        "metric": "block-sparse attention TFLOPS over kept blocks (fwd+bwd = 2.5 F)", "value": round(world * value, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) Q, K, V, dO; seeded random block mask; no dataset)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "density": w.density, "kept_blocks": int(bm.sum()), "mask_heads": int(bm.shape[0]),
+                   "flop_count": "F = 4*d per (query, key) pair inside kept blocks; fwd+bwd = 2.5 F",
+                   "l2": "inputs larger than L2 (each of Q, K, V, dO is %.0f MB > 129 MB)" % (elem / 1e6)},
+        "fwd_tflops": round(fwd, 1), "fwd_frac_of_peak": round(fwd / peak, 4),
+        "fwdbwd_frac_of_peak": round(value / peak, 4),
+        "kernel_ms": {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
+                      "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)},
+        "roofline": {"bound": "tensor", "kernel": "fa_bwd_dkdv_kernel<128,non-causal,bf16,sparse>",
+                     "achieved": round(dkdv, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(dkdv / peak, 4),
+                     "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "algorithmic": "10*d per (query, key) pair of the kept blocks (5 GEMMs), per launch"},
+        "e2e": {"value": round(world * 2.5 * F / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(4 * elem + md.numel()),
+                "d2h_bytes_per_step": int(4 * elem + w.B * w.H * w.N * 4), "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": {"value": cpu, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{heads} whole head(s) of {w.name}, float64 forward + explicit backward "
+                                   f"under the block mask, {spent:.1f} s"},
+    }
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_gpu(args, w, world, rank, local):
     import torch
@@ -396,6 +555,13 @@ def run_gpu(args, w, world, rank, local):
         dgbs = dbytes / (dms * 1e-3) / 1e9
         result["decode"] = {"workload": D1.name, "ms": round(dms, 4), "GB_per_s": round(dgbs, 1),
                             "frac_of_hbm_peak": round(dgbs / float(peaks["hbm_gbs"]), 4)}
+        from exact_io_aware_forward_gb300.synth import S1
+        sms, sparts, _, sbufs = measure_blocksparse(dev, S1, 10, 3)
+        sF = block_mask_flops(S1, sbufs[-1])
+        result["blocksparse"] = {"workload": S1.name, "ms": round(sms, 4),
+                                 "fwdbwd_tflops": round(2.5 * sF / (sms * 1e-3) / 1e12, 1),
+                                 "fwd_tflops": round(sF / (sparts[0] * 1e-3) / 1e12, 1),
+                                 "dkdv_frac_of_peak": round(2.5 * sF / (sparts[2] * 1e-3) / 1e12 / peak, 4)}
     if dist:
         dist.destroy_process_group()
     return result
@@ -434,8 +600,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="C4", help="C2, C3N, C3C, C4 or C5")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="train", choices=["train", "decode"],
-                    help="train: fwd+bwd step (the headline); decode: split-KV decoding line")
+    ap.add_argument("--mode", default="train", choices=["train", "decode", "blocksparse"],
+                    help="train: fwd+bwd step (the headline); decode: split-KV decoding line; "
+                         "blocksparse: fwd+bwd under a 128x128 block mask")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing (rank 0, N=1)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -443,10 +610,10 @@ def main():
     from exact_io_aware_forward_gb300.synth import WORKLOADS
     w = WORKLOADS[args.workload]
     world, rank, local = dist_env()
-    if args.impl == "ours" and args.mode == "decode":
+    if args.impl == "ours" and args.mode in ("decode", "blocksparse"):
         from exact_io_aware_forward_gb300 import build as fa_build
         fa_build.build()
-        out = run_decode(args, world, rank, local)
+        out = (run_decode if args.mode == "decode" else run_blocksparse)(args, world, rank, local)
         if rank == 0:
             print(json.dumps(out), flush=True)
         return

@@ -20,10 +20,15 @@ _S = ctypes.c_size_t
 SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_forward_blocksparse": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_backward_workspace_size": (_S, [_I, _I, _I, _I]),
     "fa_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _S, _P]),
+    "fa_backward_blocksparse": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _S,
+                                     _P]),
     "fa_backward_preprocess": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "fa_backward_dkdv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_backward_dkdv_blocksparse": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                          _P]),
     "fa_backward_dq_convert": (_I, [_P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),

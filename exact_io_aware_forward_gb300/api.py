@@ -76,6 +76,42 @@ def fa_forward(q, k, v, o, lse, causal=False, scale=None, stream=None) -> None:
                                           _scale(scale, d), _stream(stream)))
 
 
+def _block_mask(block_mask, B, H, N):
+    T = (N + 127) // 128
+    if not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda or block_mask.dtype != torch.uint8:
+        raise TypeError("block_mask must be a CUDA uint8 tensor")
+    if not block_mask.is_contiguous() or block_mask.dim() != 3 or tuple(block_mask.shape[1:]) != (T, T) \
+            or block_mask.shape[0] not in (1, B * H):
+        raise ValueError(f"block_mask must be contiguous [1 or B*H, {T}, {T}]")
+    return block_mask.data_ptr(), int(block_mask.shape[0])
+
+
+def fa_forward_blocksparse(q, k, v, o, lse, block_mask, causal=False, scale=None, stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    mptr, mheads = _block_mask(block_mask, B, H, N)
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt),
+            _bhnd("o", o, q.shape, dt), _bhnd("lse", lse, (B, H, N), torch.float32)]
+    _check("fa_forward_blocksparse", lib().fa_forward_blocksparse(*args, mptr, mheads, B, H, N, d, _DTYPE_CODE[dt],
+                                                                  int(bool(causal)), _scale(scale, d),
+                                                                  _stream(stream)))
+
+
+def fa_backward_blocksparse(q, k, v, o, do, lse, dq, dk, dv, block_mask, workspace, causal=False, scale=None,
+                            stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    mptr, mheads = _block_mask(block_mask, B, H, N)
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("o", o, q.shape, dt),
+            _bhnd("do", do, q.shape, dt), _bhnd("lse", lse, (B, H, N), torch.float32),
+            _bhnd("dq", dq, q.shape, dt), _bhnd("dk", dk, q.shape, dt), _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_blocksparse", lib().fa_backward_blocksparse(
+        *args, mptr, mheads, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), workspace.data_ptr(),
+        workspace.numel(), _stream(stream)))
+
+
 def fa_backward_workspace_size(B, H, N, d) -> int:
     return int(lib().fa_backward_workspace_size(B, H, N, d))
 
@@ -128,6 +164,19 @@ def fa_backward_dkdv(q, k, v, do, lse, delta, dq_accum, dk, dv, causal=False, sc
                                                       _scale(scale, d), _stream(stream)))
 
 
+def fa_backward_dkdv_blocksparse(q, k, v, do, lse, delta, dq_accum, dk, dv, block_mask, causal=False, scale=None,
+                                 stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    mptr, mheads = _block_mask(block_mask, B, H, N)
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dq_accum", dq_accum, q.shape, torch.float32), _bhnd("dk", dk, q.shape, dt),
+            _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_dkdv_blocksparse", lib().fa_backward_dkdv_blocksparse(
+        *args, mptr, mheads, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), _stream(stream)))
+
+
 def fa_backward_dq_convert(dq_accum, dq, scale=None, stream=None) -> None:
     B, H, N, d = _shape(dq)
     args = [_bhnd("dq_accum", dq_accum, dq.shape, torch.float32), _bhnd("dq", dq)]
@@ -161,12 +210,15 @@ def fa_device_status(stream=None) -> None:
 
 
 # ---------------------------------------------------------------- conveniences
-def forward(q, k, v, causal=False, scale=None, stream=None):
-    """Return (O, LSE) for [B, H, N, d] q, k, v."""
+def forward(q, k, v, causal=False, scale=None, stream=None, block_mask=None):
+    """Return (O, LSE) for [B, H, N, d] q, k, v (block-sparse if block_mask is given)."""
     B, H, N, d = _shape(q)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
-    fa_forward(q, k, v, o, lse, causal, scale, stream)
+    if block_mask is None:
+        fa_forward(q, k, v, o, lse, causal, scale, stream)
+    else:
+        fa_forward_blocksparse(q, k, v, o, lse, block_mask, causal, scale, stream)
     return o, lse
 
 
@@ -182,11 +234,14 @@ def forward_decode(q, k, v, causal=False, scale=None, num_splits=0, stream=None,
     return o, lse
 
 
-def backward(q, k, v, o, lse, do, causal=False, scale=None, stream=None, workspace=None):
-    """Return (dQ, dK, dV)."""
+def backward(q, k, v, o, lse, do, causal=False, scale=None, stream=None, workspace=None, block_mask=None):
+    """Return (dQ, dK, dV) (block-sparse if block_mask is given)."""
     B, H, N, d = _shape(q)
     if workspace is None:
         workspace = torch.empty(fa_backward_workspace_size(B, H, N, d), device=q.device, dtype=torch.uint8)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_backward(q, k, v, o, do, lse, dq, dk, dv, workspace, causal, scale, stream)
+    if block_mask is None:
+        fa_backward(q, k, v, o, do, lse, dq, dk, dv, workspace, causal, scale, stream)
+    else:
+        fa_backward_blocksparse(q, k, v, o, do, lse, dq, dk, dv, block_mask, workspace, causal, scale, stream)
     return dq, dk, dv

@@ -85,8 +85,19 @@ const char* fa_status_string(int status) {
   }
 }
 
-fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                     int d, int dtype, int causal, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status check_block_mask(const uint8_t* block_mask, int mask_heads, int B, int H) {
+  if (!block_mask) return FA_ERR_INVALID_ARG;
+  if (mask_heads != 1 && (long long)mask_heads != (long long)B * H) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
+                       int mask_heads, int B, int H, int N, int d, int dtype, int causal, float scale,
+                       void* stream) {
   fa_status st = check_shape(B, H, N, d, dtype);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
@@ -103,11 +114,30 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   a.N = N;
   a.BH = BH;
   a.scale_log2 = scale * kLog2e;
+  a.block_mask = block_mask;
+  a.mask_heads = mask_heads;
   a.status = status_word();
   if (!a.status) return FA_ERR_CUDA;
   if (fa::launch_forward(d, causal != 0, bf16, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                     int d, int dtype, int causal, float scale, void* stream) {
+  return forward_impl(q, k, v, o, lse, nullptr, 1, B, H, N, d, dtype, causal, scale, stream);
+}
+
+fa_status fa_forward_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d, int dtype,
+                                 int causal, float scale, void* stream) {
+  const fa_status st = check_block_mask(block_mask, mask_heads, B, H);
+  if (st != FA_OK) return st;
+  return forward_impl(q, k, v, o, lse, block_mask, mask_heads, B, H, N, d, dtype, causal, scale, stream);
 }
 
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
@@ -128,9 +158,13 @@ fa_status fa_backward_preprocess(const void* o, const void* dO, float* delta, fl
   return FA_OK;
 }
 
-fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                           const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N, int d,
-                           int dtype, int causal, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status dkdv_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* delta,
+                    float* dq_accum, void* dk, void* dv, const uint8_t* block_mask, int mask_heads, int B, int H,
+                    int N, int d, int dtype, int causal, float scale, void* stream) {
   fa_status st = check_shape(B, H, N, d, dtype);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
@@ -153,11 +187,33 @@ fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const vo
   a.BH = BH;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
+  a.block_mask = block_mask;
+  a.mask_heads = mask_heads;
   a.status = status_word();
   if (!a.status) return FA_ERR_CUDA;
   if (fa::launch_backward_dkdv(d, causal != 0, bf16, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                           const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N, int d,
+                           int dtype, int causal, float scale, void* stream) {
+  return dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, B, H, N, d, dtype, causal, scale, stream);
+}
+
+fa_status fa_backward_dkdv_blocksparse(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                       const float* delta, float* dq_accum, void* dk, void* dv,
+                                       const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d,
+                                       int dtype, int causal, float scale, void* stream) {
+  const fa_status st = check_block_mask(block_mask, mask_heads, B, H);
+  if (st != FA_OK) return st;
+  return dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, B, H, N, d, dtype, causal,
+                   scale, stream);
 }
 
 fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,
@@ -173,9 +229,14 @@ fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, 
   return FA_OK;
 }
 
-fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int dtype,
-                      int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status backward_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
+                        void* dq, void* dk, void* dv, const uint8_t* block_mask, int mask_heads, int B, int H, int N,
+                        int d, int dtype, int causal, float scale, void* workspace, size_t workspace_bytes,
+                        void* stream) {
   fa_status st = check_shape(B, H, N, d, dtype);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
@@ -186,10 +247,31 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   float* delta = static_cast<float*>(workspace);
   float* dq_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(float)));
   if ((st = fa_backward_preprocess(o, dO, delta, dq_accum, B, H, N, d, dtype, stream)) != FA_OK) return st;
-  if ((st = fa_backward_dkdv(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H, N, d, dtype, causal, scale,
-                             stream)) != FA_OK)
+  if ((st = dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, B, H, N, d, dtype, causal,
+                      scale, stream)) != FA_OK)
     return st;
   return fa_backward_dq_convert(dq_accum, dq, B, H, N, d, dtype, scale, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int dtype,
+                      int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, nullptr, 1, B, H, N, d, dtype, causal, scale, workspace,
+                       workspace_bytes, stream);
+}
+
+fa_status fa_backward_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                  const float* lse, void* dq, void* dk, void* dv, const uint8_t* block_mask,
+                                  int mask_heads, int B, int H, int N, int d, int dtype, int causal, float scale,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  const fa_status st = check_block_mask(block_mask, mask_heads, B, H);
+  if (st != FA_OK) return st;
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, block_mask, mask_heads, B, H, N, d, dtype, causal, scale,
+                       workspace, workspace_bytes, stream);
 }
 
 namespace {

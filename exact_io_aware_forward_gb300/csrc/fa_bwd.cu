@@ -40,7 +40,9 @@
 //               half of the epilogue.
 // Causal: query tiles entirely above the diagonal are skipped by the loop
 // bounds (the whole-block skip of section 4.5); the diagonal tile is
-// masked elementwise.
+// masked elementwise.  Block-sparse (SPARSE): query tiles whose 128-row
+// block does not keep this key tile are skipped as well; a key tile kept by
+// no query tile writes dK = dV = 0.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -150,13 +152,14 @@ __device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint4* dst,
   }
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE>
 __global__ void __launch_bounds__(640, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        void* __restrict__ dk, void* __restrict__ dv, const float* __restrict__ lse,
                        const float* __restrict__ delta, float* __restrict__ dq_accum, int N, int BH,
-                       float scale, float scale_log2, unsigned int* status) {
+                       float scale, float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads,
+                       unsigned int* status) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
   constexpr float kLog2e = 1.4426950408889634f;
@@ -196,7 +199,21 @@ __global__ void __launch_bounds__(640, 1)
   const int kv0 = j * C::BKV;
   const int n_q = (N + BQ - 1) / BQ;
   const int i_begin = CAUSAL ? kv0 / BQ : 0;
-  const int n_it = n_q - i_begin;
+  // Query tiles this key tile meets: [i_begin, n_q), and under a block mask
+  // only those whose 128-row query block keeps key tile j.  Every role walks
+  // the same sequence; `it` counts the tiles visited.
+  const uint8_t* mcol = SPARSE ? block_mask + (long long)(mask_heads == 1 ? 0 : bh) * n_kvt * n_kvt + j : nullptr;
+  auto next_tile = [&](int i) {
+    if (SPARSE)
+      while (i < n_q && mcol[(long long)((i * BQ) / C::BKV) * n_kvt] == 0) ++i;
+    return i;
+  };
+  int n_it = 0;
+  if (SPARSE) {
+    for (int i = next_tile(i_begin); i < n_q; i = next_tile(i + 1)) ++n_it;
+  } else {
+    n_it = n_q - i_begin;
+  }
   const long long head_row = (long long)bh * N;
 
   if (threadIdx.x == 0) {
@@ -245,12 +262,12 @@ __global__ void __launch_bounds__(640, 1)
         tma_load_3d(sV + s * C::KV_SLAB, &tm_v, kv_full, s * 64, kv0, bh);
       }
       int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
+      for (int it = 0, i = next_tile(i_begin); it < n_it; ++it, i = next_tile(i + 1)) {
         const int b = it % C::QS;
         const uint32_t use = (uint32_t)(it / C::QS);
         if (!mbar_wait(&q_empty[b], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         mbar_arrive_expect_tx(&q_full[b], 2 * C::Q_TILE);
-        const int q0 = (i_begin + it) * BQ;
+        const int q0 = i * BQ;
         for (int s = 0; s < C::SLABS; ++s) {
           tma_load_3d(sQ + b * C::Q_TILE + s * C::Q_SLAB, &tm_q, &q_full[b], s * 64, q0, bh);
           tma_load_3d(sDO + b * C::Q_TILE + s * C::Q_SLAB, &tm_do, &q_full[b], s * 64, q0, bh);
@@ -326,7 +343,7 @@ __global__ void __launch_bounds__(640, 1)
         }
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag, status, kStatusTimeout);
-      if (warp <= 2) {
+      if (warp <= 2 && n_it > 0) {
         if (ok) ok = mbar_wait(&q_full[0], 0, abort_flag, status, kStatusTimeout);
         if (ok) {
           tc_fence_after();
@@ -382,11 +399,12 @@ __global__ void __launch_bounds__(640, 1)
     // Per query column: -LSE*log2(e) (so that P = exp2(s*scale*log2e - LSE*log2e))
     // and -D, staged in shared memory one iteration ahead.
     float pre_l = 0.f, pre_d = 0.f;
-    auto fetch = [&](int it) {
-      const int q = (i_begin + it) * BQ + h * CW + r;
+    auto fetch = [&](int i) {  // query tile i
+      const int q = i * BQ + h * CW + r;
       if (r < CW) {
         if (q < N) {
-          pre_l = -lse[head_row + q] * kLog2e;
+          const float lq = lse[head_row + q];
+          pre_l = lq == -pos_inf() ? -pos_inf() : -lq * kLog2e;  // a row with no visible key: P = 0
           pre_d = -delta[head_row + q];
         } else {  // padding query: P = exp2(-inf) = 0
           pre_l = -pos_inf();
@@ -394,7 +412,8 @@ __global__ void __launch_bounds__(640, 1)
         }
       }
     };
-    fetch(0);
+    int i = next_tile(i_begin);
+    fetch(i);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int lb = it & 1;
@@ -408,8 +427,9 @@ __global__ void __launch_bounds__(640, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ld_full[lb]);
       if (!(ok = warp_wait(&ld_full[lb], (it >> 1) & 1, abort_flag, status))) break;
-      if (it + 1 < n_it) fetch(it + 1);
-      const int q0 = (i_begin + it) * BQ;
+      const int q0 = i * BQ;
+      i = next_tile(i + 1);
+      if (it + 1 < n_it) fetch(i);
       if (!(ok = warp_wait(sdp_full, it & 1, abort_flag, status))) break;
       tc_fence_after();
 #pragma unroll 1
@@ -477,7 +497,11 @@ __global__ void __launch_bounds__(640, 1)
       if (ok) {
         tc_fence_after();
         uint4* dst = reinterpret_cast<uint4*>(dv) + (head_row + key) * (D / 8);
-        store_rows_from_tmem<D, BF16>(lane_base + C::COL_DV, dst, key < N, 1.f);
+        if (n_it > 0) {
+          store_rows_from_tmem<D, BF16>(lane_base + C::COL_DV, dst, key < N, 1.f);
+        } else if (key < N) {  // no query tile kept this key tile (block-sparse): dV = 0
+          for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
   } else if ((warp >= 8 && warp < 12) || warp >= 16) {
@@ -489,7 +513,7 @@ __global__ void __launch_bounds__(640, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = 0, i = next_tile(i_begin); it < n_it; ++it, i = next_tile(i + 1)) {
       const int b = it % C::DQB;
       if (!(ok = warp_wait(&dq_full[b], (it / C::DQB) & 1, abort_flag, status))) break;
       tc_fence_after();
@@ -499,7 +523,7 @@ __global__ void __launch_bounds__(640, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&dq_empty[b]);
-      const int q0 = (i_begin + it) * BQ;
+      const int q0 = i * BQ;
       if (C::DQT) {  // lane = feature r, column = query q0 + 32g + c: one 128-byte line per warp and column
         float* base = dq_accum + (head_row + q0 + 32 * g) * D + r;
 #pragma unroll
@@ -519,7 +543,11 @@ __global__ void __launch_bounds__(640, 1)
         tc_fence_after();
         const int key = kv0 + r;
         uint4* dst = reinterpret_cast<uint4*>(dk) + (head_row + key) * (D / 8);
-        store_rows_from_tmem<D, BF16>(lane_base + C::COL_DK, dst, key < N, scale);
+        if (n_it > 0) {
+          store_rows_from_tmem<D, BF16>(lane_base + C::COL_DK, dst, key < N, scale);
+        } else if (key < N) {  // dK = 0 likewise
+          for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
   }
@@ -532,10 +560,10 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, BF16>;
+  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, BF16, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_kv = (a.N + C::BKV - 1) / C::BKV;
@@ -543,15 +571,21 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dk, a.dv, a.lse,
                                                          a.delta, a.dq_accum, a.N, a.BH, a.scale, a.scale_log2,
-                                                         a.status);
+                                                         a.block_mask, a.mask_heads, a.status);
   return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_dkdv_s(const BwdArgs& a, cudaStream_t stream) {
+  return a.block_mask ? launch_dkdv_t<D, CAUSAL, BF16, true>(a, stream)
+                      : launch_dkdv_t<D, CAUSAL, BF16, false>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_backward_dkdv(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream) {
 #define FA_BWD_CASE(DD, CC, BB) \
-  if (d == DD && causal == CC && bf16 == BB) return launch_dkdv_t<DD, CC, BB>(a, stream);
+  if (d == DD && causal == CC && bf16 == BB) return launch_dkdv_s<DD, CC, BB>(a, stream);
   FA_BWD_CASE(64, false, false)
   FA_BWD_CASE(64, false, true)
   FA_BWD_CASE(64, true, false)

@@ -35,6 +35,9 @@
 // Causal: key tiles entirely above the diagonal are never loaded or
 // multiplied (section 4.5's whole-block skip); the diagonal tile and the
 // ragged tail (keys >= N) are masked elementwise to -inf.
+// Block-sparse (SPARSE): the same skip driven by a mask of 128 x 128 blocks
+// (section 06 generalises the whole-block skip to any pattern); a query tile
+// that keeps no key tile writes O = 0 and LSE = -inf.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -110,12 +113,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o,
                   float* __restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
-                  unsigned int* status) {
+                  const uint8_t* __restrict__ block_mask, int mask_heads, unsigned int* status) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -142,6 +145,20 @@ __global__ void __launch_bounds__(384, 1)
   const int n_kv = (N + C::BN - 1) / C::BN;
   const int n0 = CAUSAL ? min(n_kv, q0 / C::BN + 1) : n_kv;  // key tiles seen by query tile 0
   const int n1 = CAUSAL ? min(n_kv, q0 / C::BN + 2) : n_kv;  // ... and by query tile 1
+  // Block-sparse: one mask byte per (128-row query tile, 128-key tile); a key
+  // tile is loaded only if one of the two query tiles keeps it.
+  const uint8_t* mrow0 = nullptr;
+  const uint8_t* mrow1 = nullptr;
+  bool t1_rows = true;  // query tile 1 starts inside the sequence
+  if (SPARSE) {
+    const uint8_t* mh = block_mask + (long long)(mask_heads == 1 ? 0 : bh) * n_kv * n_kv;
+    const int qt0 = q0 / C::BM;
+    t1_rows = qt0 + 1 < n_kv;
+    mrow0 = mh + (long long)qt0 * n_kv;
+    mrow1 = mh + (long long)(t1_rows ? qt0 + 1 : qt0) * n_kv;
+  }
+  auto act0 = [&](int j) { return j < n0 && (!SPARSE || mrow0[j] != 0); };
+  auto act1 = [&](int j) { return !SPARSE || (t1_rows && mrow1[j] != 0); };  // j < n1 in every loop
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -185,15 +202,34 @@ __global__ void __launch_bounds__(384, 1)
       for (int t = 0; t < C::QT; ++t)
         for (int s = 0; s < C::SLABS; ++s)
           tma_load_3d(sQ + t * C::TILE + s * C::SLAB, &tm_q, q_full, s * 64, q0 + t * C::BM, bh);
-      for (int u = 0; u < 2 * n1; ++u) {
-        const int slot = u % C::NS;
-        const uint32_t use = (uint32_t)(u / C::NS);
-        if (!mbar_wait(&ring_empty[slot], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
-        mbar_arrive_expect_tx(&ring_full[slot], C::TILE);
-        const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
-        for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, (u >> 1) * C::BN, bh);
-        issued = u + 1;
+      if constexpr (!SPARSE) {
+        for (int u = 0; u < 2 * n1; ++u) {  // K_0, V_0, K_1, V_1, ...
+          const int slot = u % C::NS;
+          const uint32_t use = (uint32_t)(u / C::NS);
+          if (!mbar_wait(&ring_empty[slot], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
+          mbar_arrive_expect_tx(&ring_full[slot], C::TILE);
+          const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
+          for (int s = 0; s < C::SLABS; ++s)
+            tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, (u >> 1) * C::BN, bh);
+          issued = u + 1;
+        }
+      } else {
+        bool ok = true;
+        for (int j = 0, u = 0; ok && j < n1; ++j) {  // u: position of key tile j in the load order
+          if (SPARSE && !act0(j) && !act1(j)) continue;
+          for (int kv = 0; kv < 2; ++kv) {
+            const int uu = 2 * u + kv;
+            const int slot = uu % C::NS;
+            const uint32_t use = (uint32_t)(uu / C::NS);
+            if (!(ok = mbar_wait(&ring_empty[slot], (use & 1) ^ 1, abort_flag, status, kStatusTimeout))) break;
+            mbar_arrive_expect_tx(&ring_full[slot], C::TILE);
+            const CUtensorMap* m = kv ? &tm_v : &tm_k;
+            for (int s = 0; s < C::SLABS; ++s)
+              tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, j * C::BN, bh);
+            issued = uu + 1;
+          }
+          ++u;
+        }
       }
       if (*abort_flag) {  // let every copy in flight land before the CTA exits
         drain_wait(q_full, 0);
@@ -218,57 +254,115 @@ __global__ void __launch_bounds__(384, 1)
                  kIdS, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int j) {
+      auto issue_pv = [&](int t, int j, bool first) {
         const uint32_t b0 = sring + vslot(j) * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           mma_ts(tmem + C::COL_O + t * D, tmem + C::COL_S + t * C::BN + kk * 8,
-                 sdesc_sw128(b0 + kk * 2048, C::SLAB, 1024), kIdPV, (j > 0 || kk > 0));
+                 sdesc_sw128(b0 + kk * 2048, C::SLAB, 1024), kIdPV, (!first || kk > 0));
         }
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusTimeout);
-      for (int j = 0; ok && j < n1; ++j) {
-        if (!(ok = mbar_wait(&ring_full[kslot(j)], kpar(j), abort_flag, status, kStatusTimeout))) break;
-        if (j >= 1 && !(ok = mbar_wait(&ring_full[vslot(j - 1)], vpar(j - 1), abort_flag, status, kStatusTimeout)))
-          break;
-        tc_fence_after();
-        if (j >= 1 && j - 1 < n0) {
-          if (!(ok = mbar_wait(&p_full[0], (j - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+      if constexpr (!SPARSE) {
+        // Per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j).  PV_t(j-1) is
+        // issued before S_t(j), whose columns hold P_t(j-1), by the same
+        // thread (in-order).
+        for (int j = 0; ok && j < n1; ++j) {
+          if (!(ok = mbar_wait(&ring_full[kslot(j)], kpar(j), abort_flag, status, kStatusTimeout))) break;
+          if (j >= 1 && !(ok = mbar_wait(&ring_full[vslot(j - 1)], vpar(j - 1), abort_flag, status, kStatusTimeout)))
+            break;
           tc_fence_after();
-          issue_pv(0, j - 1);
-        }
-        if (j < n0) {
-          issue_s(0, j);
-          mma_commit(&s_full[0]);
-        }
-        if (j >= 1) {
-          if (!(ok = mbar_wait(&p_full[1], (j - 1) & 1, abort_flag, status, kStatusTimeout))) break;
-          tc_fence_after();
-          issue_pv(1, j - 1);
-          mma_commit(&ring_empty[vslot(j - 1)]);
-        }
-        issue_s(1, j);
-        mma_commit(&s_full[1]);
-        mma_commit(&ring_empty[kslot(j)]);
-      }
-      if (ok) {
-        const int jl = n1 - 1;
-        ok = mbar_wait(&ring_full[vslot(jl)], vpar(jl), abort_flag, status, kStatusTimeout);
-        tc_fence_after();
-        if (ok && jl < n0) {
-          ok = mbar_wait(&p_full[0], jl & 1, abort_flag, status, kStatusTimeout);
-          tc_fence_after();
-          if (ok) issue_pv(0, jl);
+          if (j >= 1 && j - 1 < n0) {
+            if (!(ok = mbar_wait(&p_full[0], (j - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+            tc_fence_after();
+            issue_pv(0, j - 1, j == 1);
+          }
+          if (j < n0) {
+            issue_s(0, j);
+            mma_commit(&s_full[0]);
+          }
+          if (j >= 1) {
+            if (!(ok = mbar_wait(&p_full[1], (j - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+            tc_fence_after();
+            issue_pv(1, j - 1, j == 1);
+            mma_commit(&ring_empty[vslot(j - 1)]);
+          }
+          issue_s(1, j);
+          mma_commit(&s_full[1]);
+          mma_commit(&ring_empty[kslot(j)]);
         }
         if (ok) {
-          ok = mbar_wait(&p_full[1], jl & 1, abort_flag, status, kStatusTimeout);
+          const int jl = n1 - 1;
+          ok = mbar_wait(&ring_full[vslot(jl)], vpar(jl), abort_flag, status, kStatusTimeout);
           tc_fence_after();
+          if (ok && jl < n0) {
+            ok = mbar_wait(&p_full[0], jl & 1, abort_flag, status, kStatusTimeout);
+            tc_fence_after();
+            if (ok) issue_pv(0, jl, jl == 0);
+          }
           if (ok) {
-            issue_pv(1, jl);
-            mma_commit(o_full);
+            ok = mbar_wait(&p_full[1], jl & 1, abort_flag, status, kStatusTimeout);
+            tc_fence_after();
+            if (ok) issue_pv(1, jl, jl == 0);
+          }
+        }
+      } else {
+        // Per load-order position u: PV_0(prev), S_0(u), PV_1(prev), S_1(u), where
+        // prev is the previous position; a query tile skips the products of the
+        // key tiles it does not keep.  PV_t(prev) is issued before S_t(u), whose
+        // columns hold P_t(prev), by the same thread (in-order).
+        int prev = -1, c0 = 0, c1 = 0;  // previous position; S products issued per tile
+        bool pa0 = false, pa1 = false;  // tile t kept the key tile at prev
+        for (int j = 0, u = 0; ok && j < n1; ++j) {
+          const bool a0 = act0(j), a1 = act1(j);
+          if (SPARSE && !a0 && !a1) continue;
+          if (prev >= 0 && !(ok = mbar_wait(&ring_full[vslot(prev)], vpar(prev), abort_flag, status, kStatusTimeout)))
+            break;
+          if (pa0) {
+            if (!(ok = mbar_wait(&p_full[0], (c0 - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+            tc_fence_after();
+            issue_pv(0, prev, c0 == 1);
+          }
+          if (!(ok = mbar_wait(&ring_full[kslot(u)], kpar(u), abort_flag, status, kStatusTimeout))) break;
+          tc_fence_after();
+          if (a0) {
+            issue_s(0, u);
+            mma_commit(&s_full[0]);
+            ++c0;
+          }
+          if (pa1) {
+            if (!(ok = mbar_wait(&p_full[1], (c1 - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+            tc_fence_after();
+            issue_pv(1, prev, c1 == 1);
+          }
+          if (prev >= 0) mma_commit(&ring_empty[vslot(prev)]);
+          if (a1) {
+            issue_s(1, u);
+            mma_commit(&s_full[1]);
+            ++c1;
+          }
+          mma_commit(&ring_empty[kslot(u)]);
+          prev = u;
+          pa0 = a0;
+          pa1 = a1;
+          ++u;
+        }
+        if (ok && prev >= 0) {
+          ok = mbar_wait(&ring_full[vslot(prev)], vpar(prev), abort_flag, status, kStatusTimeout);
+          tc_fence_after();
+          if (ok && pa0) {
+            ok = mbar_wait(&p_full[0], (c0 - 1) & 1, abort_flag, status, kStatusTimeout);
+            tc_fence_after();
+            if (ok) issue_pv(0, prev, c0 == 1);
+          }
+          if (ok && pa1) {
+            ok = mbar_wait(&p_full[1], (c1 - 1) & 1, abort_flag, status, kStatusTimeout);
+            tc_fence_after();
+            if (ok) issue_pv(1, prev, c1 == 1);
           }
         }
       }
+      if (ok) mma_commit(o_full);
       if (!ok) {  // every MMA issued so far must finish before TMEM is freed
         mma_commit(drain);
         drain_wait(drain, 0);
@@ -289,31 +383,37 @@ __global__ void __launch_bounds__(384, 1)
     float l = 0.f;            // sum of exp2(score - m_ref): gives LSE
     float l_mma = 0.f;        // the same sum over P rounded to 16 bit: normalises O
     bool ok = true;
+    int c = 0;  // key tiles processed so far by this query tile
     for (int j = 0; j < n_t; ++j) {
-      if (!(ok = warp_wait(&s_full[t], j & 1, abort_flag, status))) break;
+      if constexpr (SPARSE) {
+        if (!(t == 0 ? act0(j) : act1(j))) continue;
+      } else {
+        c = j;
+      }
+      if (!(ok = warp_wait(&s_full[t], c & 1, abort_flag, status))) break;
       tc_fence_after();
       float s[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, s[cc]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(s[cc]);
 
       const int kbase = j * C::BN;
       const bool need_mask = (kbase + C::BN > N) || (CAUSAL && kbase + C::BN - 1 > q0 + t * C::BM);
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = kbase + 32 * c + i;
-            if (key >= N || (CAUSAL && key > row)) s[c][i] = neg_inf();
+            const int key = kbase + 32 * cc + i;
+            if (key >= N || (CAUSAL && key > row)) s[cc][i] = neg_inf();
           }
       }
       float mx = s[0][0];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) mx = max3(mx, s[c][i], s[c][i + 1]);
+        for (int i = 0; i < 32; i += 2) mx = max3(mx, s[cc][i], s[cc][i + 1]);
       const float m_new = fmaxf(m_ref, mx * scale_log2);
       float corr = 1.f;
       bool rescale_o = false;
@@ -322,7 +422,7 @@ __global__ void __launch_bounds__(384, 1)
         corr = ex2_approx(m_ref - m_use);
         l *= corr;
         l_mma *= corr;
-        rescale_o = j > 0;
+        rescale_o = c > 0;
         m_ref = m_use;
       }
       const float neg_m = (m_ref == neg_inf()) ? 0.f : -m_ref;
@@ -331,12 +431,12 @@ __global__ void __launch_bounds__(384, 1)
       uint64_t sum2 = f2_pack(0.f, 0.f);   // sum of P as computed (fp32)
       uint64_t sumr2 = f2_pack(0.f, 0.f);  // sum of P as rounded for the MMA
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 scores -> 16 packed pairs -> 16 TMEM columns
+      for (int cc = 0; cc < 4; ++cc) {  // 32 scores -> 16 packed pairs -> 16 TMEM columns
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[c][2 * i], s[c][2 * i + 1]), sc2, nm2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(s[cc][2 * i], s[cc][2 * i + 1]), sc2, nm2), x0, x1);
           const float p0 = ex2_approx(x0);
           const float p1 = ex2_approx(x1);
           sum2 = f2_add(sum2, f2_pack(p0, p1));
@@ -345,13 +445,13 @@ __global__ void __launch_bounds__(384, 1)
           unpack2(pk[i], BF16, r0, r1);
           sumr2 = f2_add(sumr2, f2_pack(r0, r1));
         }
-        tmem_st16(tS + 16 * c, pk);
+        tmem_st16(tS + 16 * cc, pk);
       }
       if (rescale_o) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
-          tmem_ld32(tO + 32 * c, o);
+          tmem_ld32(tO + 32 * cc, o);
           tmem_ld_wait(o);
           const uint64_t corr2 = f2_pack(corr, corr);
           uint32_t ou[32];
@@ -362,7 +462,7 @@ __global__ void __launch_bounds__(384, 1)
             ou[i] = __float_as_uint(a);
             ou[i + 1] = __float_as_uint(b);
           }
-          tmem_st32(tO + 32 * c, ou);
+          tmem_st32(tO + 32 * cc, ou);
         }
       }
       tmem_st_wait();
@@ -374,11 +474,18 @@ __global__ void __launch_bounds__(384, 1)
       l += a + b;
       f2_unpack(sumr2, a, b);
       l_mma += a + b;
+      ++c;
     }
 
     // ------------------------------------------------------------ epilogue
     if (ok) ok = warp_wait(o_full, 0, abort_flag, status);
-    if (ok) {
+    if (SPARSE && ok && c == 0) {  // no key tile kept: empty softmax, O = 0, LSE = -inf
+      uint4* orow = reinterpret_cast<uint4*>(o) + ((long long)bh * N + row) * (D / 8);
+      if (row < N) {
+        for (int q = 0; q < D / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
+        lse[(long long)bh * N + row] = neg_inf();
+      }
+    } else if (ok) {
       tc_fence_after();
       // O is divided by the sum of the rounded weights that entered the MMA,
       // so each output row stays a convex combination of V rows; the
@@ -388,16 +495,16 @@ __global__ void __launch_bounds__(384, 1)
       // Each thread writes its own row: D/8 16-byte chunks, contiguous in memory.
       uint4* orow = reinterpret_cast<uint4*>(o) + ((long long)bh * N + row) * (D / 8);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         float ov[32];
-        tmem_ld32(tO + 32 * c, ov);
+        tmem_ld32(tO + 32 * cc, ov);
         tmem_ld_wait(ov);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, BF16);
         if (row < N) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) orow[4 * c + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) orow[4 * cc + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
       if (row < N) {
@@ -415,25 +522,30 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, BF16>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, BF16, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblocks = (a.N + C::QT * C::BM - 1) / (C::QT * C::BM);
   const long long grid = (long long)n_qblocks * a.BH;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.N, a.BH,
-                                                         n_qblocks, a.scale_log2, a.status);
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.N, a.BH, n_qblocks,
+                                                         a.scale_log2, a.block_mask, a.mask_heads, a.status);
   return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_fwd_s(const FwdArgs& a, cudaStream_t stream) {
+  return a.block_mask ? launch_fwd_t<D, CAUSAL, BF16, true>(a, stream) : launch_fwd_t<D, CAUSAL, BF16, false>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream) {
 #define FA_FWD_CASE(DD, CC, BB) \
-  if (d == DD && causal == CC && bf16 == BB) return launch_fwd_t<DD, CC, BB>(a, stream);
+  if (d == DD && causal == CC && bf16 == BB) return launch_fwd_s<DD, CC, BB>(a, stream);
   FA_FWD_CASE(64, false, false)
   FA_FWD_CASE(64, false, true)
   FA_FWD_CASE(64, true, false)

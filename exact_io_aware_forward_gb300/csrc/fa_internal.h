@@ -18,6 +18,8 @@ struct FwdArgs {
   int N;
   int BH;
   float scale_log2;                    // scale * log2(e)
+  const uint8_t* block_mask = nullptr; // [mask_heads, T, T] block mask, T = ceil(N/128); null = dense
+  int mask_heads = 1;                  // 1 (shared by all heads) or B*H
   unsigned int* status;                // device status word
 };
 cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
@@ -34,6 +36,8 @@ struct BwdArgs {
   int BH;
   float scale;
   float scale_log2;
+  const uint8_t* block_mask = nullptr;  // as FwdArgs
+  int mask_heads = 1;
   unsigned int* status;
 };
 int backward_q_tile(int d);  // query rows per inner iteration of the dK/dV kernel

@@ -122,6 +122,49 @@ def decode_inputs(w: DecodeWorkload):
     return q, k, v
 
 
+@dataclasses.dataclass(frozen=True)
+class BlockSparseWorkload:
+    """Attention restricted to the kept 128 x 128 blocks of a block mask."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str
+    causal: bool
+    density: float  # probability that an off-diagonal block is kept
+    per_head: bool  # one mask per (b, h) head, else one mask for all heads
+    seed: int
+
+    @property
+    def tiles(self) -> int:
+        return (self.N + 127) // 128
+
+
+def block_mask(w: BlockSparseWorkload) -> np.ndarray:
+    """Boolean mask [1 or B*H, T, T], T = ceil(N/128): each block kept with
+    probability ``density``, the diagonal block always kept, drawn from
+    ``numpy.random.default_rng(seed)``."""
+    T = w.tiles
+    rng = np.random.default_rng(w.seed)
+    bm = rng.random((w.B * w.H if w.per_head else 1, T, T)) < w.density
+    bm[:, np.arange(T), np.arange(T)] = True
+    return bm
+
+
+# Block-sparse workload: the shape of the long causal training problem with a
+# random half of the off-diagonal blocks kept, one mask shared by all heads.
+S1 = BlockSparseWorkload("S1 block-sparse density 0.5 N=8192 d=128 bf16", 2, 32, 8192, 128, "bf16", False, 0.5,
+                         False, 7)
+
+
+def blocksparse_inputs(w: BlockSparseWorkload):
+    """(q, k, v, dO [B,H,N,d], mask [1 or B*H, T, T] bool)."""
+    q, k, v, do = attention_inputs(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed)
+    return q, k, v, do, block_mask(w)
+
+
 def page_inputs(N: int, D: int, seed: int):
     """float64 Q, K, V of one head, drawn like the tutorial page's demos."""
     rng = np.random.default_rng(seed)

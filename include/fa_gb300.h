@@ -42,6 +42,7 @@
 #define FA_GB300_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -73,6 +74,22 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      int d, int dtype, int causal, float scale, void* stream);
 
 /*
+ * Block-sparse forward: fa_forward with whole 128 x 128 (query, key) blocks
+ * removed.  The tutorial's section 06 generalises the causal whole-block skip
+ * to any sparsity pattern; kept blocks are computed exactly as in
+ * fa_forward, removed blocks are never loaded or multiplied.
+ * block_mask: DEVICE pointer to uint8 [mask_heads, T, T], T = ceil(N/128),
+ * row-major; nonzero = keep the block (query block i, key block j).
+ * mask_heads: 1 (one mask for every head) or B*H (one per head, in [B,H]
+ * order).  `causal` still applies inside kept blocks.  A query row that keeps
+ * no key at all gets O = 0 and LSE = -inf.  Errors: FA_ERR_INVALID_ARG for a
+ * null mask or a mask_heads other than 1 or B*H; otherwise as fa_forward.
+ */
+fa_status fa_forward_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d, int dtype,
+                                 int causal, float scale, void* stream);
+
+/*
  * Bytes of device workspace fa_backward needs: D (B*H*N float32) followed by
  * the float32 dQ accumulator (B*H*N*d float32), each 256-byte aligned.
  * Linear in N.  Returns 0 for invalid sizes.
@@ -95,6 +112,17 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
                       int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Block-sparse backward: fa_backward for the forward of
+ * fa_forward_blocksparse with the same block_mask / mask_heads / causal.
+ * Products of removed blocks are skipped; a key block kept by no query block
+ * gets dK = dV = 0, a query row with no visible key gets dQ = 0.
+ */
+fa_status fa_backward_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                  const float* lse, void* dq, void* dk, void* dv, const uint8_t* block_mask,
+                                  int mask_heads, int B, int H, int N, int d, int dtype, int causal, float scale,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Stage 1 of the backward pass: D_i = sum_c dO_ic * O_ic in float32 (the
  * row-sum shortcut for rowsum(P * (dO V^T)), which holds because O = P V),
  * and dq_accum := 0.  delta: [B,H,N] float32 out; dq_accum: [B,H,N,d]
@@ -113,6 +141,17 @@ fa_status fa_backward_preprocess(const void* o, const void* dO, float* delta, fl
 fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                            const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N, int d,
                            int dtype, int causal, float scale, void* stream);
+
+/*
+ * Stage 2 of fa_backward_blocksparse: fa_backward_dkdv restricted to the
+ * kept blocks of block_mask (same mask arguments and errors as
+ * fa_forward_blocksparse).  A key block kept by no query block gets
+ * dK = dV = 0 and adds nothing to dq_accum.
+ */
+fa_status fa_backward_dkdv_blocksparse(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                       const float* delta, float* dq_accum, void* dk, void* dv,
+                                       const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d,
+                                       int dtype, int causal, float scale, void* stream);
 
 /* Stage 3: dq = scale * dq_accum, rounded to dtype. */
 fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,

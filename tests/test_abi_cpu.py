@@ -95,3 +95,21 @@ def test_decode_workspace_and_validation(lib):
     assert rc == 1
     rc = lib.fa_forward_decode(ptr, ptr, ptr, ptr, ptr, 1, 1, 2, 4, 64, 1, 0, 0.125, 0, ptr, 16, None)
     assert rc == 5
+
+
+def test_blocksparse_mask_validation(lib):
+    """A null mask or a mask count that is neither 1 nor B*H is rejected
+    before any launch, in all three block-sparse entry points."""
+    ptr = 1 << 20
+    for mask, heads in ((None, 1), (ptr, 0), (ptr, 5)):
+        rc = lib.fa_forward_blocksparse(ptr, ptr, ptr, ptr, ptr, mask, heads, 2, 3, 300, 64, 1, 0, 0.125, None)
+        assert rc == 1
+        rc = lib.fa_backward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, mask, heads, 2, 3, 300, 64, 1,
+                                         0, 0.125, ptr, 1 << 30, None)
+        assert rc == 1
+        rc = lib.fa_backward_dkdv_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, mask, heads, 2, 3, 300, 64,
+                                              1, 0, 0.125, None)
+        assert rc == 1
+    # shape errors still come first with a valid mask count
+    rc = lib.fa_forward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, 6, 2, 3, 300, 96, 1, 0, 0.125, None)
+    assert rc == 2
