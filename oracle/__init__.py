@@ -13,6 +13,8 @@ Modules
                the explicit softmax backward).
 ``online``     an independent streaming (online-softmax) evaluation used only
                to pin ``attention`` against the recurrence the pages derive.
+``dropout``    the Philox4x32-10 counter-based generator (written from its
+               published definition) and the keep mask it defines.
 
 Every function cites the page passage it follows.  Pages are named by title:
 
@@ -24,7 +26,10 @@ Parity pins (all under ``tests/test_oracle*.py``): the page's worked trace
 rescale ablation (P3 section 09), the causal block count (P3 section 04.5),
 closed forms (uniform scores, causal row 0, N = 1), an independent
 log-sum-exp, torch's float64 CPU attention and autograd, central finite
-differences, and the backward invariants that follow from P3 section 3.3.
+differences, the backward invariants that follow from P3 section 3.3, and
+for dropout the generator's published known-answer values, a per-entry
+scalar evaluation of the counter mapping, binomial bounds on the keep
+fraction, and torch float64 autograd with the keep mask as a constant.
 No function is "parity unpinned".
 """
-from . import attention, online  # noqa: F401
+from . import attention, dropout, online  # noqa: F401

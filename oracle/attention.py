@@ -25,6 +25,14 @@ Definitions followed
   scores.  A query row with no visible key at all has no softmax; the
   reading taken is O = 0 and LSE = -inf for it (and no gradient flows).
 
+* Dropout (P3 section 05: the mask is regenerated from the generator's seed
+  and offset, never stored): with a boolean keep mask Z and the keep scale
+  c = 1 / keep probability, the forward pass uses P~ = P * Z * c in place of
+  P, so O = P~ V, while LSE stays the softmax normaliser of the undropped
+  scores.  Backward: dV = P~^T G; the gradient reaching P is
+  dP = (G V^T) * Z * c, and dS = P * (dP - rowsum(dP * P)).  Z itself comes
+  from ``oracle.dropout``.
+
 Arrays are numpy float64.  Batched entry points take [B, H, N, d] arrays and
 loop over heads; the ``*_head`` functions take one head [N, d].
 """
@@ -82,12 +90,21 @@ def _softmax_backward(p, a):
 # --------------------------------------------------------------------------
 # one head
 # --------------------------------------------------------------------------
-def forward_head(q, k, v, scale, causal=False, rows=None, block_mask=None):
-    """O and LSE of one head ([N, d] inputs) for the query rows ``rows``."""
+def _dropped(p, keep, keep_scale):
+    """P~ = P * Z * c (P itself when there is no dropout)."""
+    if keep is None:
+        return p
+    return np.where(keep, p * keep_scale, 0.0)
+
+
+def forward_head(q, k, v, scale, causal=False, rows=None, block_mask=None, keep=None, keep_scale=1.0):
+    """O and LSE of one head ([N, d] inputs) for the query rows ``rows``.
+
+    ``keep`` (boolean [rows, Nk]) and ``keep_scale`` apply dropout to P."""
     s = _scores(q, k, scale, causal, rows, block_mask)
     p, m, l = _softmax_rows(s)
     with np.errstate(divide="ignore"):
-        return p @ v, m + np.log(l)
+        return _dropped(p, keep, keep_scale) @ v, m + np.log(l)
 
 
 def probabilities_head(q, k, scale, causal=False, rows=None):
@@ -96,14 +113,17 @@ def probabilities_head(q, k, scale, causal=False, rows=None):
     return p
 
 
-def backward_head(q, k, v, do, scale, causal=False, block_mask=None):
-    """(dQ, dK, dV) of one head, everything materialised (P3 section 3.3)."""
+def backward_head(q, k, v, do, scale, causal=False, block_mask=None, keep=None, keep_scale=1.0):
+    """(dQ, dK, dV) of one head, everything materialised (P3 section 3.3).
+
+    With dropout (``keep``, ``keep_scale``) the gradient reaching P is
+    (dO V^T) * Z * c and dV = P~^T dO."""
     p, _, _ = _softmax_rows(_scores(q, k, scale, causal, block_mask=block_mask))
-    a = do @ v.T
+    a = _dropped(do @ v.T, keep, keep_scale)
     ds = _softmax_backward(p, a)
     dq = scale * (ds @ k)
     dk = scale * (ds.T @ q)
-    dv = p.T @ do
+    dv = _dropped(p, keep, keep_scale).T @ do
     return dq, dk, dv
 
 
