@@ -17,6 +17,8 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _S = ctypes.c_size_t
+_U64 = ctypes.c_uint64
+_U32 = ctypes.c_uint32
 SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
@@ -33,6 +35,12 @@ SIGNATURES = {
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
     "fa_forward_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "fa_forward_dropout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32, _P]),
+    "fa_backward_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32, _P,
+                                 _S, _P]),
+    "fa_backward_dkdv_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32,
+                                      _P]),
+    "fa_dropout_keep_mask": (_I, [_P, _I, _I, _I, _F, _U64, _U32, _P]),
     "fa_device_status": (_I, [_P]),
 }
 

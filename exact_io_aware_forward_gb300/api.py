@@ -112,6 +112,64 @@ def fa_backward_blocksparse(q, k, v, o, do, lse, dq, dk, dv, block_mask, workspa
         workspace.numel(), _stream(stream)))
 
 
+def _seed_offset(seed, offset):
+    seed, offset = int(seed), int(offset)
+    if not (0 <= seed < 2**64 and 0 <= offset < 2**32):
+        raise ValueError("seed must fit 64 bits and offset 32 bits (unsigned)")
+    return seed, offset
+
+
+def fa_forward_dropout(q, k, v, o, lse, p_drop, seed, offset, causal=False, scale=None, stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    seed, offset = _seed_offset(seed, offset)
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt),
+            _bhnd("o", o, q.shape, dt), _bhnd("lse", lse, (B, H, N), torch.float32)]
+    _check("fa_forward_dropout", lib().fa_forward_dropout(*args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)),
+                                                          _scale(scale, d), float(p_drop), seed, offset,
+                                                          _stream(stream)))
+
+
+def fa_backward_dropout(q, k, v, o, do, lse, dq, dk, dv, workspace, p_drop, seed, offset, causal=False, scale=None,
+                        stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    seed, offset = _seed_offset(seed, offset)
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("o", o, q.shape, dt),
+            _bhnd("do", do, q.shape, dt), _bhnd("lse", lse, (B, H, N), torch.float32),
+            _bhnd("dq", dq, q.shape, dt), _bhnd("dk", dk, q.shape, dt), _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_dropout", lib().fa_backward_dropout(
+        *args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), float(p_drop), seed, offset,
+        workspace.data_ptr(), workspace.numel(), _stream(stream)))
+
+
+def fa_backward_dkdv_dropout(q, k, v, do, lse, delta, dq_accum, dk, dv, p_drop, seed, offset, causal=False,
+                             scale=None, stream=None) -> None:
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    seed, offset = _seed_offset(seed, offset)
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dq_accum", dq_accum, q.shape, torch.float32), _bhnd("dk", dk, q.shape, dt),
+            _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_dkdv_dropout", lib().fa_backward_dkdv_dropout(
+        *args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), float(p_drop), seed, offset,
+        _stream(stream)))
+
+
+def fa_dropout_keep_mask(keep, p_drop, seed, offset, stream=None) -> None:
+    """Write the keep mask ([BH, Nq, Nk] uint8 CUDA tensor, 1 = kept) the dropout entry points use."""
+    if not isinstance(keep, torch.Tensor) or not keep.is_cuda or keep.dtype != torch.uint8 \
+            or not keep.is_contiguous() or keep.dim() != 3:
+        raise TypeError("keep must be a contiguous CUDA uint8 tensor [BH, Nq, Nk]")
+    seed, offset = _seed_offset(seed, offset)
+    BH, Nq, Nk = keep.shape
+    _check("fa_dropout_keep_mask", lib().fa_dropout_keep_mask(keep.data_ptr(), BH, Nq, Nk, float(p_drop), seed,
+                                                              offset, _stream(stream)))
+
+
 def fa_backward_workspace_size(B, H, N, d) -> int:
     return int(lib().fa_backward_workspace_size(B, H, N, d))
 
@@ -210,12 +268,17 @@ def fa_device_status(stream=None) -> None:
 
 
 # ---------------------------------------------------------------- conveniences
-def forward(q, k, v, causal=False, scale=None, stream=None, block_mask=None):
-    """Return (O, LSE) for [B, H, N, d] q, k, v (block-sparse if block_mask is given)."""
+def forward(q, k, v, causal=False, scale=None, stream=None, block_mask=None, dropout_p=0.0, seed=0, offset=0):
+    """Return (O, LSE) for [B, H, N, d] q, k, v (block-sparse if block_mask is
+    given; with dropout on P if dropout_p > 0, keep mask drawn from seed and offset)."""
     B, H, N, d = _shape(q)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
-    if block_mask is None:
+    if dropout_p and block_mask is not None:
+        raise ValueError("dropout is supported for dense attention only")
+    if dropout_p:
+        fa_forward_dropout(q, k, v, o, lse, dropout_p, seed, offset, causal, scale, stream)
+    elif block_mask is None:
         fa_forward(q, k, v, o, lse, causal, scale, stream)
     else:
         fa_forward_blocksparse(q, k, v, o, lse, block_mask, causal, scale, stream)
@@ -234,13 +297,19 @@ def forward_decode(q, k, v, causal=False, scale=None, num_splits=0, stream=None,
     return o, lse
 
 
-def backward(q, k, v, o, lse, do, causal=False, scale=None, stream=None, workspace=None, block_mask=None):
-    """Return (dQ, dK, dV) (block-sparse if block_mask is given)."""
+def backward(q, k, v, o, lse, do, causal=False, scale=None, stream=None, workspace=None, block_mask=None,
+             dropout_p=0.0, seed=0, offset=0):
+    """Return (dQ, dK, dV) (block-sparse if block_mask is given; with the
+    forward's dropout if dropout_p > 0 -- pass the same seed and offset)."""
     B, H, N, d = _shape(q)
     if workspace is None:
         workspace = torch.empty(fa_backward_workspace_size(B, H, N, d), device=q.device, dtype=torch.uint8)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    if block_mask is None:
+    if dropout_p and block_mask is not None:
+        raise ValueError("dropout is supported for dense attention only")
+    if dropout_p:
+        fa_backward_dropout(q, k, v, o, do, lse, dq, dk, dv, workspace, dropout_p, seed, offset, causal, scale, stream)
+    elif block_mask is None:
         fa_backward(q, k, v, o, do, lse, dq, dk, dv, workspace, causal, scale, stream)
     else:
         fa_backward_blocksparse(q, k, v, o, do, lse, dq, dk, dv, block_mask, workspace, causal, scale, stream)

@@ -89,6 +89,21 @@ const char* fa_status_string(int status) {
 
 namespace {
 
+// Dropout probability -> generator parameters: t = round(p * 65536), keep
+// scale 65536 / (65536 - t).  False for p outside [0, 1) (NaN included) or
+// p rounding to 1.
+bool make_drop(float p, uint64_t seed, uint32_t offset, fa::DropParams* dp) {
+  if (!(p >= 0.f && p < 1.f)) return false;
+  const double t = floor((double)p * 65536.0 + 0.5);
+  if (t >= 65536.0) return false;
+  dp->t = (uint32_t)t;
+  dp->keep_scale = (float)(65536.0 / (65536.0 - t));
+  dp->k0 = (uint32_t)(seed & 0xffffffffu);
+  dp->k1 = (uint32_t)(seed >> 32);
+  dp->offset = offset;
+  return true;
+}
+
 fa_status check_block_mask(const uint8_t* block_mask, int mask_heads, int B, int H) {
   if (!block_mask) return FA_ERR_INVALID_ARG;
   if (mask_heads != 1 && (long long)mask_heads != (long long)B * H) return FA_ERR_INVALID_ARG;
@@ -97,7 +112,7 @@ fa_status check_block_mask(const uint8_t* block_mask, int mask_heads, int B, int
 
 fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
                        int mask_heads, int B, int H, int N, int d, int dtype, int causal, float scale,
-                       void* stream) {
+                       void* stream, const fa::DropParams* drop = nullptr) {
   fa_status st = check_shape(B, H, N, d, dtype);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
@@ -118,8 +133,12 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
   a.mask_heads = mask_heads;
   a.status = status_word();
   if (!a.status) return FA_ERR_CUDA;
-  if (fa::launch_forward(d, causal != 0, bf16, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FA_ERR_CUDA;
+  // p rounding to 0 drops nothing: the plain kernel computes exactly that.
+  a.dropout = drop != nullptr && drop->t > 0;
+  if (a.dropout) a.drop = *drop;
+  const cudaError_t e = a.dropout ? fa::launch_forward_dropout(d, causal != 0, bf16, a, static_cast<cudaStream_t>(stream))
+                                  : fa::launch_forward(d, causal != 0, bf16, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 
@@ -164,7 +183,8 @@ namespace {
 
 fa_status dkdv_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* delta,
                     float* dq_accum, void* dk, void* dv, const uint8_t* block_mask, int mask_heads, int B, int H,
-                    int N, int d, int dtype, int causal, float scale, void* stream) {
+                    int N, int d, int dtype, int causal, float scale, void* stream,
+                    const fa::DropParams* drop = nullptr) {
   fa_status st = check_shape(B, H, N, d, dtype);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
@@ -191,8 +211,12 @@ fa_status dkdv_impl(const void* q, const void* k, const void* v, const void* dO,
   a.mask_heads = mask_heads;
   a.status = status_word();
   if (!a.status) return FA_ERR_CUDA;
-  if (fa::launch_backward_dkdv(d, causal != 0, bf16, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FA_ERR_CUDA;
+  a.dropout = drop != nullptr && drop->t > 0;
+  if (a.dropout) a.drop = *drop;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = a.dropout ? fa::launch_backward_dkdv_dropout(d, causal != 0, bf16, a, s)
+                                  : fa::launch_backward_dkdv(d, causal != 0, bf16, a, s);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 
@@ -236,7 +260,7 @@ namespace {
 fa_status backward_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                         void* dq, void* dk, void* dv, const uint8_t* block_mask, int mask_heads, int B, int H, int N,
                         int d, int dtype, int causal, float scale, void* workspace, size_t workspace_bytes,
-                        void* stream) {
+                        void* stream, const fa::DropParams* drop = nullptr) {
   fa_status st = check_shape(B, H, N, d, dtype);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
@@ -248,7 +272,7 @@ fa_status backward_impl(const void* q, const void* k, const void* v, const void*
   float* dq_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(float)));
   if ((st = fa_backward_preprocess(o, dO, delta, dq_accum, B, H, N, d, dtype, stream)) != FA_OK) return st;
   if ((st = dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, B, H, N, d, dtype, causal,
-                      scale, stream)) != FA_OK)
+                      scale, stream, drop)) != FA_OK)
     return st;
   return fa_backward_dq_convert(dq_accum, dq, B, H, N, d, dtype, scale, stream);
 }
@@ -330,6 +354,44 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o
   a.o_part = static_cast<float*>(workspace);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)));
   if (fa::launch_decode(d, dtype == FA_BF16, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                             int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                             uint32_t offset, void* stream) {
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return forward_impl(q, k, v, o, lse, nullptr, 1, B, H, N, d, dtype, causal, scale, stream, &dp);
+}
+
+fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int dtype,
+                              int causal, float scale, float p_drop, uint64_t seed, uint32_t offset, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, nullptr, 1, B, H, N, d, dtype, causal, scale, workspace,
+                       workspace_bytes, stream, &dp);
+}
+
+fa_status fa_backward_dkdv_dropout(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                   const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N,
+                                   int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                                   uint32_t offset, void* stream) {
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, B, H, N, d, dtype, causal, scale, stream,
+                   &dp);
+}
+
+fa_status fa_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, float p_drop, uint64_t seed, uint32_t offset,
+                               void* stream) {
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  if (BH < 1 || Nq < 1 || Nk < 1 || !keep) return FA_ERR_INVALID_ARG;
+  if (fa::launch_dropout_keep_mask(keep, BH, Nq, Nk, dp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }

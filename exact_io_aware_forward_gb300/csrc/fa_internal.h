@@ -11,6 +11,15 @@ namespace fa {
 // Status bits latched by kernels in the device status word.
 constexpr unsigned int kStatusTimeout = 1u;
 
+// Dropout parameters (see fa_philox.cuh): entries whose 16-bit draw is below
+// t are dropped; kept ones are scaled by keep_scale = 65536 / (65536 - t).
+struct DropParams {
+  uint32_t t = 0;
+  float keep_scale = 1.f;
+  uint32_t k0 = 0, k1 = 0;  // generator key: seed low and high words
+  uint32_t offset = 0;      // counter word 3
+};
+
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;        // 3-D maps over [B*H, N, d], box {64, 128, 1}
   void* o;                             // [B*H, N, d]
@@ -20,9 +29,12 @@ struct FwdArgs {
   float scale_log2;                    // scale * log2(e)
   const uint8_t* block_mask = nullptr; // [mask_heads, T, T] block mask, T = ceil(N/128); null = dense
   int mask_heads = 1;                  // 1 (shared by all heads) or B*H
+  bool dropout = false;                // apply `drop` (dense attention only)
+  DropParams drop;
   unsigned int* status;                // device status word
 };
 cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_forward_dropout(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_do;         // box {64, BQ, 1}
@@ -38,10 +50,16 @@ struct BwdArgs {
   float scale_log2;
   const uint8_t* block_mask = nullptr;  // as FwdArgs
   int mask_heads = 1;
+  bool dropout = false;                 // as FwdArgs
+  DropParams drop;
   unsigned int* status;
 };
 int backward_q_tile(int d);  // query rows per inner iteration of the dK/dV kernel
 cudaError_t launch_backward_dkdv(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_backward_dkdv_dropout(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream);
+// keep[bh][i][j] = 1 if entry (bh, i, j) is kept, else 0 ([BH, Nq, Nk] bytes).
+cudaError_t launch_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, const DropParams& drop,
+                                     cudaStream_t stream);
 cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const void* dO, float* delta,
                                        float* dq_accum, long long rows, cudaStream_t stream);
 cudaError_t launch_backward_dq_convert(int d, bool bf16, const float* dq_accum, void* dq, long long rows,

@@ -123,6 +123,45 @@ fa_status fa_backward_blocksparse(const void* q, const void* k, const void* v, c
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Attention dropout ("FlashAttention 为什么不需要存下注意力矩阵", section 05: the
+ * kernel stores no dropout mask, only the seed and offset of a Philox
+ * counter-based generator, and the backward pass regenerates the mask).
+ *
+ * The dropout acts on the normalised probabilities: O = (P * Z / (1 - p')) V
+ * with Z the keep mask and p' = t / 65536, t = round(p_drop * 65536) (p_drop
+ * is quantised to 2^-16); lse is still the log-sum-exp of the undropped
+ * scores.  Z is drawn with Philox4x32-10 (Salmon et al., SC 2011): entry
+ * (head bh = b*H + h, query i, key j) uses counter (j / 8, i, bh, offset)
+ * and key (seed & 0xffffffff, seed >> 32); word (j / 2) % 4 of the output
+ * gives a 16-bit draw (low half for even j, high half for odd j), and the
+ * entry is kept iff draw >= t.  The same (p_drop, seed, offset) must be
+ * passed to the backward call; a new offset (or seed) gives a new mask.
+ * p_drop must be in [0, 1) and not round to 1, else FA_ERR_INVALID_ARG;
+ * p_drop rounding to 0 computes plain attention.  Dense attention only
+ * (no block mask).  Other arguments, errors and layouts as fa_forward /
+ * fa_backward / fa_backward_dkdv.
+ */
+fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                             int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                             uint32_t offset, void* stream);
+fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int dtype,
+                              int causal, float scale, float p_drop, uint64_t seed, uint32_t offset, void* workspace,
+                              size_t workspace_bytes, void* stream);
+fa_status fa_backward_dkdv_dropout(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                   const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N,
+                                   int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                                   uint32_t offset, void* stream);
+
+/*
+ * The keep mask the dropout entry points use, written out: keep is a device
+ * buffer of BH * Nq * Nk bytes ([BH, Nq, Nk], 1 = kept, 0 = dropped).  For
+ * inspection and tests; the attention entry points never store it.
+ */
+fa_status fa_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, float p_drop, uint64_t seed, uint32_t offset,
+                               void* stream);
+
+/*
  * Stage 1 of the backward pass: D_i = sum_c dO_ic * O_ic in float32 (the
  * row-sum shortcut for rowsum(P * (dO V^T)), which holds because O = P V),
  * and dq_accum := 0.  delta: [B,H,N] float32 out; dq_accum: [B,H,N,d]

@@ -113,3 +113,20 @@ def test_blocksparse_mask_validation(lib):
     # shape errors still come first with a valid mask count
     rc = lib.fa_forward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, 6, 2, 3, 300, 96, 1, 0, 0.125, None)
     assert rc == 2
+
+
+def test_dropout_validation(lib):
+    """p outside [0, 1), NaN, or rounding to 1 is rejected before any launch."""
+    ptr = 1 << 20
+    for p in (-0.1, 1.0, float("nan"), 1.0 - 2 ** -18):
+        rc = lib.fa_forward_dropout(ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125, p, 1, 0, None)
+        assert rc == 1, p
+        rc = lib.fa_backward_dropout(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125, p, 1, 0,
+                                     ptr, 1 << 30, None)
+        assert rc == 1, p
+        rc = lib.fa_backward_dkdv_dropout(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125, p,
+                                          1, 0, None)
+        assert rc == 1, p
+        assert lib.fa_dropout_keep_mask(ptr, 1, 4, 4, p, 1, 0, None) == 1
+    assert lib.fa_dropout_keep_mask(None, 1, 4, 4, 0.5, 1, 0, None) == 1
+    assert lib.fa_dropout_keep_mask(ptr, 0, 4, 4, 0.5, 1, 0, None) == 1
