@@ -430,8 +430,36 @@ __global__ void __launch_bounds__(640, 1)
         }
       }
     };
+    // Dropout keep bits of this thread's key for the CW query columns of the
+    // next tile (bit 16 sc + c <-> query column 16 sc + c of this warpgroup),
+    // drawn after the previous tile's P / dS are handed over, off the path
+    // from S^T to P^T.  Lane 8g + r8 draws queries c0 + r8 and c0 + 8 + r8
+    // for the 8 keys of its group; an 8 x 8 bit transpose across the group
+    // gives each lane the bits of its own key (key offset r8).
+    uint32_t kw0 = 0u, kw1 = 0u;  // columns 0-31, 32-63
+    auto draw_keep = [&](int q0n) {
+      const uint32_t kgrp = (uint32_t)(key >> 3);
+      const int r8 = lane & 7;
+#pragma unroll
+      for (int sc = 0; sc < CW / 16; ++sc) {
+        const int c0 = q0n + h * CW + 16 * sc;
+        const uint4 w0 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + r8), (uint32_t)bh, drop.offset), drop.k0,
+                                       drop.k1);
+        const uint4 w1 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + 8 + r8), (uint32_t)bh, drop.offset),
+                                       drop.k0, drop.k1);
+        uint32_t x = keep_byte(w0, drop.t) | (keep_byte(w1, drop.t) << 8);
+        x = transpose8_step(x, lane, 4, 0x0F0Fu);
+        x = transpose8_step(x, lane, 2, 0x3333u);
+        x = transpose8_step(x, lane, 1, 0x5555u);
+        if (sc == 0) kw0 = x;
+        if (sc == 1) kw0 |= x << 16;
+        if (sc == 2) kw1 = x;
+        if (sc == 3) kw1 |= x << 16;
+      }
+    };
     int i = next_tile(i_begin);
     fetch(i);
+    if (DROP && n_it > 0) draw_keep(i * BQ);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int lb = it & 1;
@@ -465,21 +493,7 @@ __global__ void __launch_bounds__(640, 1)
         }
         const int c0 = q0 + col;  // first query of this sub-chunk
         const bool need_mask = (CAUSAL && c0 < kv0 + C::BKV - 1) || (kv0 + C::BKV > N);
-        uint32_t keep = 0xffffu;  // bit c: entry (query c0 + c, this key) kept
-        if (DROP) {
-          // Lane 8g + r8 draws queries c0 + r8 and c0 + 8 + r8 for the 8 keys of its group ...
-          const uint32_t kgrp = (uint32_t)(key >> 3);
-          const int r8 = lane & 7;
-          const uint4 w0 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + r8), (uint32_t)bh, drop.offset), drop.k0,
-                                         drop.k1);
-          const uint4 w1 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + 8 + r8), (uint32_t)bh, drop.offset),
-                                         drop.k0, drop.k1);
-          keep = keep_byte(w0, drop.t) | (keep_byte(w1, drop.t) << 8);
-          // ... and the transpose gives it the bits of its own key (key offset r8) for all 16 queries.
-          keep = transpose8_step(keep, lane, 4, 0x0F0Fu);
-          keep = transpose8_step(keep, lane, 2, 0x3333u);
-          keep = transpose8_step(keep, lane, 1, 0x5555u);
-        }
+        const uint32_t keep = DROP ? (((sc >> 1) ? kw1 : kw0) >> (16 * (sc & 1))) : 0xffffu;  // bit c: (c0 + c, key) kept
         uint32_t pp[8], dd[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -533,6 +547,7 @@ __global__ void __launch_bounds__(640, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pds_full[pb]);
+      if (DROP && it + 1 < n_it) draw_keep(i * BQ);  // i is already the next tile
     }
     if (h == 0) {
       if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);

@@ -394,6 +394,11 @@ __global__ void __launch_bounds__(384, 1)
     float l_mma = 0.f;        // the same sum over P rounded to 16 bit: normalises O
     bool ok = true;
     int c = 0;  // key tiles processed so far by this query tile
+    // Dropout keep bits of the next key tile (tiles are visited in order
+    // 0, 1, ... when DROP): drawn while the tensor core works, so that the
+    // generator stays off the path from S to P.
+    uint32_t keep[4] = {0u, 0u, 0u, 0u};
+    if (DROP && n_t > 0) tile_keep_bits(keep, 0, row, bh, drop.offset, drop.k0, drop.k1, drop.t);
     for (int j = 0; j < n_t; ++j) {
       if constexpr (SPARSE) {
         if (!(t == 0 ? act0(j) : act1(j))) continue;
@@ -455,17 +460,9 @@ __global__ void __launch_bounds__(384, 1)
           unpack2(pk[i], BF16, r0, r1);
           sumr2 = f2_add(sumr2, f2_pack(r0, r1));
         }
-        if (DROP) {  // keys kbase + 32cc .. +31: four generator calls of 8 keys each
+        if (DROP) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint4 w = philox4x32_10(
-                make_uint4((uint32_t)((kbase + 32 * cc) >> 3) + g, (uint32_t)row, (uint32_t)bh, drop.offset),
-                drop.k0, drop.k1);
-            pk[4 * g + 0] &= keep_halves(w.x, drop.t);  // word r holds keys 2r, 2r+1 of the call
-            pk[4 * g + 1] &= keep_halves(w.y, drop.t);
-            pk[4 * g + 2] &= keep_halves(w.z, drop.t);
-            pk[4 * g + 3] &= keep_halves(w.w, drop.t);
-          }
+          for (int i = 0; i < 16; ++i) pk[i] &= pair_keep_mask(keep[cc], i);
         }
         tmem_st16(tS + 16 * cc, pk);
       }
@@ -491,6 +488,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
+      if (DROP && j + 1 < n_t) tile_keep_bits(keep, (j + 1) * C::BN, row, bh, drop.offset, drop.k0, drop.k1, drop.t);
       float a, b;
       f2_unpack(sum2, a, b);
       l += a + b;

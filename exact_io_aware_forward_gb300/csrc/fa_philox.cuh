@@ -35,24 +35,52 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// 0xffff in each 16-bit half of w whose draw is kept (>= t), 0 elsewhere: a
-// mask that zeroes the dropped element of a packed 16-bit pair.
-__device__ __forceinline__ uint32_t keep_halves(uint32_t w, uint32_t t) {
-  const uint32_t lo = (w & 0xffffu) >= t ? 0x0000ffffu : 0u;
-  const uint32_t hi = (w >> 16) >= t ? 0xffff0000u : 0u;
-  return lo | hi;
-}
-
 // Keep bits of the 8 keys of one generator call: bit k <-> key 8 * (j / 8) + k.
+// __vsetgeu2 gives 1 in each 16-bit half whose draw is >= t.
 __device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t t) {
-  uint32_t b = 0;
+  const uint32_t tt = t | (t << 16);
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  uint32_t b = 0;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    b |= ((ws[r] & 0xffffu) >= t ? 1u : 0u) << (2 * r);
-    b |= ((ws[r] >> 16) >= t ? 1u : 0u) << (2 * r + 1);
+    const uint32_t v = __vsetgeu2(ws[r], tt);
+    b |= ((v & 1u) | ((v >> 15) & 2u)) << (2 * r);
   }
   return b;
+}
+
+// Keep bits of the 128 keys [kbase, kbase + 128) of query `row`, one word per
+// 32 keys: in word cc, bit i is the even key kbase + 32cc + 2i of pair i and
+// bit 16 + i the odd key kbase + 32cc + 2i + 1 (16 generator calls).
+__device__ __forceinline__ void tile_keep_bits(uint32_t (&eo)[4], int kbase, int row, int bh, uint32_t offset,
+                                               uint32_t k0, uint32_t k1, uint32_t t) {
+  const uint32_t tt = t | (t << 16);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t e = 0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint4 w = philox4x32_10(
+          make_uint4(((uint32_t)(kbase + 32 * cc) >> 3) + g, (uint32_t)row, (uint32_t)bh, offset), k0, k1);
+      // __vsetgeu2: 1 in each 16-bit half whose draw is >= t, i.e. bit 0 (even
+      // key) and bit 16 (odd key) of the pair held by word r.
+      e |= __vsetgeu2(w.x, tt) << (4 * g + 0);
+      e |= __vsetgeu2(w.y, tt) << (4 * g + 1);
+      e |= __vsetgeu2(w.z, tt) << (4 * g + 2);
+      e |= __vsetgeu2(w.w, tt) << (4 * g + 3);
+    }
+    eo[cc] = e;
+  }
+}
+
+// 0xffff over each kept half of packed pair i from a keep word of
+// tile_keep_bits: bits i and 16 + i are moved to bits 7 and 23, and prmt
+// replicates the top bit of bytes 0 and 2 over the low and high halves.
+__device__ __forceinline__ uint32_t pair_keep_mask(uint32_t eo, int i) {
+  const uint32_t x = i <= 7 ? eo << (7 - i) : eo >> (i - 7);
+  uint32_t m;
+  asm("prmt.b32 %0, %1, 0, 0xAA88;" : "=r"(m) : "r"(x));
+  return m;
 }
 
 }  // namespace fa
