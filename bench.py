@@ -267,20 +267,29 @@ def block_mask_flops(w, bm) -> float:
     return 4.0 * w.d * float(total)
 
 
-def oracle_blocksparse_sample(w, bm, budget_s: float, max_heads: int):
-    """float64 oracle (forward + explicit backward under the block mask) on
-    whole heads until `budget_s` is spent; TFLOP/s in the 2.5 F convention."""
+def oracle_variant_sample(kind, w, bm, budget_s: float, max_heads: int):
+    """float64 oracle (forward + explicit backward) on whole heads of a
+    block-sparse or dropout workload until `budget_s` is spent; TFLOP/s in the
+    2.5 F convention, F counted like the GPU line."""
     from exact_io_aware_forward_gb300.synth import as_float64, attention_inputs
     from oracle import attention as A
+    from oracle import dropout as DR
     heads, spent, flops = 0, 0.0, 0.0
     scale = 1.0 / math.sqrt(w.d)
-    per_head = block_mask_flops(w, bm) / (w.B * w.H)  # average over heads
+    per_head = (block_mask_flops(w, bm) if kind == "blocksparse" else w.fwd_flops()) / (w.B * w.H)
     while heads < max_heads and (heads == 0 or spent < budget_s):
         q, k, v, do = as_float64(*attention_inputs(1, 1, w.N, w.d, w.dtype, seed=w.seed * 1000 + heads))
-        m = bm[0 if bm.shape[0] == 1 else heads % bm.shape[0]]
+        q, k, v, do = q[0, 0], k[0, 0], v[0, 0], do[0, 0]
         t0 = time.perf_counter()
-        A.forward_head(q[0, 0], k[0, 0], v[0, 0], scale, w.causal, block_mask=m)
-        A.backward_head(q[0, 0], k[0, 0], v[0, 0], do[0, 0], scale, w.causal, block_mask=m)
+        if kind == "blocksparse":
+            m = bm[0 if bm.shape[0] == 1 else heads % bm.shape[0]]
+            A.forward_head(q, k, v, scale, w.causal, block_mask=m)
+            A.backward_head(q, k, v, do, scale, w.causal, block_mask=m)
+        else:  # the keep mask is part of the method: drawn inside the timed region
+            keep = DR.keep_mask(DROP_SEED, DROP_OFFSET, DROP_P, heads, w.N, w.N)
+            c = DR.keep_scale(DROP_P)
+            A.forward_head(q, k, v, scale, w.causal, keep=keep, keep_scale=c)
+            A.backward_head(q, k, v, do, scale, w.causal, keep=keep, keep_scale=c)
         spent += time.perf_counter() - t0
         flops += 2.5 * per_head
         heads += 1
@@ -288,17 +297,26 @@ def oracle_blocksparse_sample(w, bm, budget_s: float, max_heads: int):
     return flops / spent / 1e12, heads, spent, threads
 
 
-def measure_blocksparse(dev, w, steps, warmup, sampler=None):
-    """Device-resident fwd+bwd under the block mask, each of the four kernels
-    timed with CUDA events on the launching stream."""
+# Dropout line: the long causal training workload with p = 0.1.
+DROP_P, DROP_SEED, DROP_OFFSET = 0.1, 2024, 0
+
+
+def measure_variant(dev, kind, w, steps, warmup, sampler=None):
+    """Device-resident fwd+bwd of a block-sparse or dropout workload, each of
+    the four kernels timed with CUDA events on the launching stream.
+    Returns (ms per step, per-kernel ms, clocks, buffers)."""
     import torch
 
     import exact_io_aware_forward_gb300 as fa
-    from exact_io_aware_forward_gb300.synth import blocksparse_inputs
+    from exact_io_aware_forward_gb300.synth import blocksparse_inputs, workload_inputs
 
-    q, k, v, do, bm = blocksparse_inputs(w)
+    if kind == "blocksparse":
+        q, k, v, do, bm = blocksparse_inputs(w)
+        md = torch.from_numpy(bm.astype("uint8")).to(dev)
+    else:
+        q, k, v, do = workload_inputs(w)
+        bm = md = None
     q, k, v, do = (x.to(dev) for x in (q, k, v, do))
-    md = torch.from_numpy(bm.astype("uint8")).to(dev)
     B, H, N, d = w.B, w.H, w.N, w.d
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
@@ -311,13 +329,26 @@ def measure_blocksparse(dev, w, steps, warmup, sampler=None):
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
 
+    def fwd():
+        if kind == "blocksparse":
+            fa.fa_forward_blocksparse(q, k, v, o, lse, md, w.causal)
+        else:
+            fa.fa_forward_dropout(q, k, v, o, lse, DROP_P, DROP_SEED, DROP_OFFSET, w.causal)
+
+    def dkdv():
+        if kind == "blocksparse":
+            fa.fa_backward_dkdv_blocksparse(q, k, v, do, lse, delta, acc, dk, dv, md, w.causal)
+        else:
+            fa.fa_backward_dkdv_dropout(q, k, v, do, lse, delta, acc, dk, dv, DROP_P, DROP_SEED, DROP_OFFSET,
+                                        w.causal)
+
     def step(e=None):
         if e: e[0].record(stream)
-        fa.fa_forward_blocksparse(q, k, v, o, lse, md, w.causal)
+        fwd()
         if e: e[1].record(stream)
         fa.fa_backward_preprocess(o, do, delta, acc)
         if e: e[2].record(stream)
-        fa.fa_backward_dkdv_blocksparse(q, k, v, do, lse, delta, acc, dk, dv, md, w.causal)
+        dkdv()
         if e: e[3].record(stream)
         fa.fa_backward_dq_convert(acc, dq)
         if e: e[4].record(stream)
@@ -341,28 +372,38 @@ def measure_blocksparse(dev, w, steps, warmup, sampler=None):
     return t0.elapsed_time(t1) / steps, parts, clocks, (q, k, v, do, md, ws, bm)
 
 
-def run_blocksparse(args, world, rank, local):
+def variant_flops(kind, w, bm):
+    return block_mask_flops(w, bm) if kind == "blocksparse" else w.fwd_flops()
+
+
+def run_variant(args, world, rank, local, kind):
+    """The JSON line of `--mode blocksparse` (S1) or `--mode dropout` (C4 with p = 0.1)."""
     import torch
 
     import exact_io_aware_forward_gb300 as fa
-    from exact_io_aware_forward_gb300.synth import S1 as w
+    from exact_io_aware_forward_gb300.synth import C4, S1
 
+    w = S1 if kind == "blocksparse" else C4
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
-    ms, parts, clocks, (q, k, v, do, md, ws, bm) = measure_blocksparse(dev, w, args.steps, args.warmup,
-                                                                         ClockSampler(local))
-    F = block_mask_flops(w, bm)
+    ms, parts, clocks, (q, k, v, do, md, ws, bm) = measure_variant(dev, kind, w, args.steps, args.warmup,
+                                                                   ClockSampler(local))
+    F = variant_flops(kind, w, bm)
     value = 2.5 * F / (ms * 1e-3) / 1e12
     hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
-    hm = md.cpu().pin_memory()
+    hm = md.cpu().pin_memory() if md is not None else None
     ho, hdq, hdk, hdv = (torch.empty_like(x, device="cpu").pin_memory() for x in (q, q, q, q))
     hlse = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    extra = {"block_mask": None} if kind == "blocksparse" else \
+        {"dropout_p": DROP_P, "seed": DROP_SEED, "offset": DROP_OFFSET}
 
     def e2e_step():
-        gq, gk, gv, gdo, gm = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, hdo, hm))
-        go, glse = fa.forward(gq, gk, gv, causal=w.causal, block_mask=gm)
-        gdq, gdk, gdv = fa.backward(gq, gk, gv, go, glse, gdo, causal=w.causal, workspace=ws, block_mask=gm)
+        gq, gk, gv, gdo = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, hdo))
+        if kind == "blocksparse":
+            extra["block_mask"] = hm.to(dev, non_blocking=True)
+        go, glse = fa.forward(gq, gk, gv, causal=w.causal, **extra)
+        gdq, gdk, gdv = fa.backward(gq, gk, gv, go, glse, gdo, causal=w.causal, workspace=ws, **extra)
         for h, g in ((ho, go), (hlse, glse), (hdq, gdq), (hdk, gdk), (hdv, gdv)):
             h.copy_(g, non_blocking=True)
 
@@ -380,32 +421,47 @@ def run_blocksparse(args, world, rank, local):
     peak = float(peaks["bf16_tflops"])
     dkdv = 2.5 * F / (parts[2] * 1e-3) / 1e12
     fwd = F / (parts[0] * 1e-3) / 1e12
-    cpu, heads, spent, threads = oracle_blocksparse_sample(w, bm, args.cpu_budget, 64)
+    cpu, heads, spent, threads = oracle_variant_sample(kind, w, bm, args.cpu_budget, 64)
+    if kind == "blocksparse":
+        metric = "block-sparse attention TFLOPS over kept blocks (fwd+bwd = 2.5 F)"
+        data = "synthetic (seeded N(0,1) Q, K, V, dO; seeded random block mask; no dataset)"
+        cfg = {"density": w.density, "kept_blocks": int(bm.sum()), "mask_heads": int(bm.shape[0]),
+               "flop_count": "F = 4*d per (query, key) pair inside kept blocks; fwd+bwd = 2.5 F"}
+        kern = "fa_bwd_dkdv_kernel<128,non-causal,bf16,sparse>"
+        alg = "10*d per (query, key) pair of the kept blocks (5 GEMMs), per launch"
+        h2d_extra = md.numel()
+        what = "under the block mask"
+    else:
+        metric = "attention TFLOPS with dropout regenerated from (seed, offset) (fwd+bwd = 2.5 F)"
+        data = "synthetic (seeded N(0,1) Q, K, V, dO; no dataset)"
+        cfg = {"dropout_p": DROP_P, "seed": DROP_SEED, "offset": DROP_OFFSET,
+               "flop_count": "fwd+bwd = 2.5 * 4*B*H*N^2*d (halved causal); generator work not counted"}
+        kern = "fa_bwd_dkdv_kernel<128,causal,bf16,dropout>"
+        alg = "10*N^2*d per head (5 GEMMs), halved causal, per launch"
+        h2d_extra = 0
+        what = "with the keep mask drawn by the oracle's generator"
     return {
-        "metric": "block-sparse attention TFLOPS over kept blocks (fwd+bwd = 2.5 F)", "value": round(world * value, 2),
+        "metric": metric, "value": round(world * value, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic (seeded N(0,1) Q, K, V, dO; seeded random block mask; no dataset)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-                   "density": w.density, "kept_blocks": int(bm.sum()), "mask_heads": int(bm.shape[0]),
-                   "flop_count": "F = 4*d per (query, key) pair inside kept blocks; fwd+bwd = 2.5 F",
-                   "l2": "inputs larger than L2 (each of Q, K, V, dO is %.0f MB > 129 MB)" % (elem / 1e6)},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": data,
+        "config": dict({"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                        "l2": "inputs larger than L2 (each of Q, K, V, dO is %.0f MB > 129 MB)" % (elem / 1e6)},
+                       **cfg),
         "fwd_tflops": round(fwd, 1), "fwd_frac_of_peak": round(fwd / peak, 4),
         "fwdbwd_frac_of_peak": round(value / peak, 4),
         "kernel_ms": {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
                       "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)},
-        "roofline": {"bound": "tensor", "kernel": "fa_bwd_dkdv_kernel<128,non-causal,bf16,sparse>",
+        "roofline": {"bound": "tensor", "kernel": kern,
                      "achieved": round(dkdv, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(dkdv / peak, 4),
-                     "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                     "algorithmic": "10*d per (query, key) pair of the kept blocks (5 GEMMs), per launch"},
+                     "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic": alg},
         "e2e": {"value": round(world * 2.5 * F / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": int(4 * elem + md.numel()),
+                "h2d_bytes_per_step": int(4 * elem + h2d_extra),
                 "d2h_bytes_per_step": int(4 * elem + w.B * w.H * w.N * 4), "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "cpu_baseline": {"value": cpu, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{heads} whole head(s) of {w.name}, float64 forward + explicit backward "
-                                   f"under the block mask, {spent:.1f} s"},
+                                   f"{what}, {spent:.1f} s"},
     }
 
 
@@ -556,12 +612,13 @@ def run_gpu(args, w, world, rank, local):
         result["decode"] = {"workload": D1.name, "ms": round(dms, 4), "GB_per_s": round(dgbs, 1),
                             "frac_of_hbm_peak": round(dgbs / float(peaks["hbm_gbs"]), 4)}
         from exact_io_aware_forward_gb300.synth import S1
-        sms, sparts, _, sbufs = measure_blocksparse(dev, S1, 10, 3)
-        sF = block_mask_flops(S1, sbufs[-1])
-        result["blocksparse"] = {"workload": S1.name, "ms": round(sms, 4),
-                                 "fwdbwd_tflops": round(2.5 * sF / (sms * 1e-3) / 1e12, 1),
-                                 "fwd_tflops": round(sF / (sparts[0] * 1e-3) / 1e12, 1),
-                                 "dkdv_frac_of_peak": round(2.5 * sF / (sparts[2] * 1e-3) / 1e12 / peak, 4)}
+        for kind, vw in (("blocksparse", S1), ("dropout", w)):
+            sms, sparts, _, sbufs = measure_variant(dev, kind, vw, 10, 3)
+            sF = variant_flops(kind, vw, sbufs[-1])
+            result[kind] = {"workload": vw.name + (f" p={DROP_P}" if kind == "dropout" else ""),
+                            "ms": round(sms, 4), "fwdbwd_tflops": round(2.5 * sF / (sms * 1e-3) / 1e12, 1),
+                            "fwd_tflops": round(sF / (sparts[0] * 1e-3) / 1e12, 1),
+                            "dkdv_frac_of_peak": round(2.5 * sF / (sparts[2] * 1e-3) / 1e12 / peak, 4)}
     if dist:
         dist.destroy_process_group()
     return result
@@ -600,9 +657,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="C4", help="C2, C3N, C3C, C4 or C5")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="train", choices=["train", "decode", "blocksparse"],
+    ap.add_argument("--mode", default="train", choices=["train", "decode", "blocksparse", "dropout"],
                     help="train: fwd+bwd step (the headline); decode: split-KV decoding line; "
-                         "blocksparse: fwd+bwd under a 128x128 block mask")
+                         "blocksparse: fwd+bwd under a 128x128 block mask; dropout: fwd+bwd of the "
+                         "training workload with dropout p=0.1")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing (rank 0, N=1)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -610,10 +668,13 @@ def main():
     from exact_io_aware_forward_gb300.synth import WORKLOADS
     w = WORKLOADS[args.workload]
     world, rank, local = dist_env()
-    if args.impl == "ours" and args.mode in ("decode", "blocksparse"):
+    if args.impl == "ours" and args.mode in ("decode", "blocksparse", "dropout"):
         from exact_io_aware_forward_gb300 import build as fa_build
         fa_build.build()
-        out = (run_decode if args.mode == "decode" else run_blocksparse)(args, world, rank, local)
+        if args.mode == "decode":
+            out = run_decode(args, world, rank, local)
+        else:
+            out = run_variant(args, world, rank, local, args.mode)
         if rank == 0:
             print(json.dumps(out), flush=True)
         return
