@@ -15,6 +15,8 @@ Modules
                to pin ``attention`` against the recurrence the pages derive.
 ``dropout``    the Philox4x32-10 counter-based generator (written from its
                published definition) and the keep mask it defines.
+``varlen``     packed variable-length sequences: each sequence an independent
+               problem, bottom-right causal alignment when Nq != Nk.
 
 Every function cites the page passage it follows.  Pages are named by title:
 
@@ -32,4 +34,4 @@ scalar evaluation of the counter mapping, binomial bounds on the keep
 fraction, and torch float64 autograd with the keep mask as a constant.
 No function is "parity unpinned".
 """
-from . import attention, dropout, online  # noqa: F401
+from . import attention, dropout, online, varlen  # noqa: F401
