@@ -170,6 +170,76 @@ def fa_dropout_keep_mask(keep, p_drop, seed, offset, stream=None) -> None:
                                                               offset, _stream(stream)))
 
 
+# ---------------------------------------------------------------- packed variable-length batches
+def _varlen_args(q, k, cu_seqlens_q, cu_seqlens_k):
+    if q.dim() != 3 or k.dim() != 3 or q.shape[1:] != k.shape[1:]:
+        raise ValueError("q must be [total_q, H, d] and k, v [total_k, H, d]")
+    if q.dtype not in _DTYPE_CODE:
+        raise TypeError("q must be float16 or bfloat16")
+    for name, cu in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if not isinstance(cu, torch.Tensor) or not cu.is_cuda or cu.dtype != torch.int32 or not cu.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 offsets")
+    B = cu_seqlens_q.numel() - 1
+    Tq, H, d = q.shape
+    return B, H, d, Tq, k.shape[0]
+
+
+def fa_forward_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False,
+                      scale=None, dropout_p=0.0, seed=0, offset=0, stream=None) -> None:
+    B, H, d, Tq, Tk = _varlen_args(q, k, cu_seqlens_q, cu_seqlens_k)
+    dt = q.dtype
+    seed, offset = _seed_offset(seed, offset)
+    args = [_bhnd("q", q), _bhnd("k", k, k.shape, dt), _bhnd("v", v, k.shape, dt), _bhnd("o", o, q.shape, dt),
+            _bhnd("lse", lse, (Tq, H), torch.float32), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr()]
+    _check("fa_forward_varlen", lib().fa_forward_varlen(
+        *args, B, H, int(max_seqlen_q), int(max_seqlen_k), Tq, Tk, d, _DTYPE_CODE[dt], int(bool(causal)),
+        _scale(scale, d), float(dropout_p), seed, offset, _stream(stream)))
+
+
+def fa_backward_varlen_workspace_size(total_q, H, d) -> int:
+    return int(lib().fa_backward_varlen_workspace_size(int(total_q), int(H), int(d)))
+
+
+def fa_backward_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                       workspace, causal=False, scale=None, dropout_p=0.0, seed=0, offset=0, stream=None) -> None:
+    B, H, d, Tq, Tk = _varlen_args(q, k, cu_seqlens_q, cu_seqlens_k)
+    dt = q.dtype
+    seed, offset = _seed_offset(seed, offset)
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    args = [_bhnd("q", q), _bhnd("k", k, k.shape, dt), _bhnd("v", v, k.shape, dt), _bhnd("o", o, q.shape, dt),
+            _bhnd("do", do, q.shape, dt), _bhnd("lse", lse, (Tq, H), torch.float32), _bhnd("dq", dq, q.shape, dt),
+            _bhnd("dk", dk, k.shape, dt), _bhnd("dv", dv, k.shape, dt), cu_seqlens_q.data_ptr(),
+            cu_seqlens_k.data_ptr()]
+    _check("fa_backward_varlen", lib().fa_backward_varlen(
+        *args, B, H, int(max_seqlen_q), int(max_seqlen_k), Tq, Tk, d, _DTYPE_CODE[dt], int(bool(causal)),
+        _scale(scale, d), float(dropout_p), seed, offset, workspace.data_ptr(), workspace.numel(), _stream(stream)))
+
+
+def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False, scale=None,
+                   dropout_p=0.0, seed=0, offset=0, stream=None):
+    """Return (O [total_q, H, d], LSE [total_q, H]) for packed sequences."""
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], q.shape[1]), device=q.device, dtype=torch.float32)
+    fa_forward_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, scale,
+                      dropout_p, seed, offset, stream)
+    return o, lse
+
+
+def backward_varlen(q, k, v, o, lse, do, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False,
+                    scale=None, dropout_p=0.0, seed=0, offset=0, stream=None, workspace=None):
+    """Return (dQ, dK, dV) for packed sequences (same arguments as the forward)."""
+    if workspace is None:
+        n = fa_backward_varlen_workspace_size(q.shape[0], q.shape[1], q.shape[2])
+        workspace = torch.empty(max(n, 1), device=q.device, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_backward_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                       workspace, causal, scale, dropout_p, seed, offset, stream)
+    return dq, dk, dv
+
+
 def fa_backward_workspace_size(B, H, N, d) -> int:
     return int(lib().fa_backward_workspace_size(B, H, N, d))
 

@@ -32,62 +32,116 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D tiled map over a contiguous [BH, N, d] 16-bit tensor: box of 64 columns
-// x `box_rows` rows x 1 head, 128-byte swizzle, out-of-range rows read as 0.
-bool make_map(CUtensorMap* m, const void* ptr, bool bf16, int d, int N, int BH, int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-fa_status check_shape(int B, int H, int N, int d, int dtype) {
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  const long long elems = (long long)B * H * N * d;
-  if (elems >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
-  return FA_OK;
-}
-
-fa_status check_scale(float scale) {
-  return (isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID_ARG;
-}
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-}  // namespace
-
-extern "C" {
-
-const char* fa_status_string(int status) {
-  switch (status) {
-    case FA_OK: return "FA_OK";
-    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null/misaligned pointer, bad size or bad scale";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128, dtype fp16/bf16, B*H*N*d < 2^31";
-    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA launch or the stream failed";
-    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up waiting on its pipeline";
-    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned or too small";
-    case FA_ERR_SCRATCH_TOO_SMALL:
-      return "FA_ERR_SCRATCH_TOO_SMALL: fa_backward_noalloc needs more than its fixed 32 MiB scratch; use fa_backward";
-    default: return "unknown fa_status";
-  }
+fa_status check_scale(float scale) {
+  return (isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID_ARG;
 }
 
-}  // extern "C"
+// One attention problem as the kernels see it: head dimension, dtype and the
+// row layout (dense [B, H, N, d] or packed variable-length [T, H, d]).
+struct Shape {
+  int B = 0, H = 0, d = 0, dtype = 0;
+  fa::SeqLayout lay;
+  bool varlen() const { return lay.cu_q != nullptr; }
+  long long q_rows() const { return varlen() ? (long long)lay.Tq * H : (long long)B * H * lay.Nq; }
+  bool bf16() const { return dtype == FA_BF16; }
+  int width() const { return d == 64 ? 64 : 128; }  // compute width of the kernels (96 runs at 128)
+};
 
-namespace {
+fa_status check_dims(int d, int dtype) {
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status dense_shape(int B, int H, int Nq, int Nk, int d, int dtype, Shape* s) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  const fa_status st = check_dims(d, dtype);
+  if (st != FA_OK) return st;
+  const long long BH = (long long)B * H;
+  if (BH * Nq * d >= (1LL << 31) || BH * Nk * d >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+  s->B = B;
+  s->H = H;
+  s->d = d;
+  s->dtype = dtype;
+  s->lay = fa::SeqLayout();
+  s->lay.H = H;
+  s->lay.Nq = Nq;
+  s->lay.Nk = Nk;
+  s->lay.dh = d;
+  return FA_OK;
+}
+
+fa_status varlen_shape(const int* cu_q, const int* cu_k, int B, int H, int max_q, int max_k, int total_q,
+                       int total_k, int d, int dtype, Shape* s) {
+  if (!cu_q || !cu_k || (reinterpret_cast<uintptr_t>(cu_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_k) & 3u))
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || max_q < 1 || max_k < 1 || total_q < 1 || total_k < 1) return FA_ERR_INVALID_ARG;
+  const fa_status st = check_dims(d, dtype);
+  if (st != FA_OK) return st;
+  if ((long long)total_q * H * d >= (1LL << 31) || (long long)total_k * H * d >= (1LL << 31))
+    return FA_ERR_UNSUPPORTED;
+  s->B = B;
+  s->H = H;
+  s->d = d;
+  s->dtype = dtype;
+  s->lay = fa::SeqLayout();
+  s->lay.cu_q = cu_q;
+  s->lay.cu_k = cu_k;
+  s->lay.H = H;
+  s->lay.Nq = max_q;
+  s->lay.Nk = max_k;
+  s->lay.Tq = total_q;
+  s->lay.Tk = total_k;
+  s->lay.dh = d;
+  return FA_OK;
+}
+
+// 3-D tiled TMA map over the query-side (key_side = false) or key-side rows
+// of `s`: boxes of 64 columns x `box_rows` rows, 128-byte swizzle; rows and
+// columns out of range read as 0 (d = 96: columns 96-127 of the second box).
+//   dense:  dims (d, N, B*H), box {64, box_rows, 1}
+//   varlen: dims (d, H, T),   box {64, 1, box_rows}  (strides increase)
+bool make_map(CUtensorMap* m, const void* ptr, const Shape& s, bool key_side, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t d = (cuuint64_t)s.d;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  if (s.varlen()) {
+    const cuuint64_t T = (cuuint64_t)(key_side ? s.lay.Tk : s.lay.Tq);
+    dims[0] = d;
+    dims[1] = (cuuint64_t)s.H;
+    dims[2] = T;
+    strides[0] = d * 2;
+    strides[1] = (cuuint64_t)s.H * d * 2;
+    box[0] = 64;
+    box[1] = 1;
+    box[2] = (cuuint32_t)box_rows;
+  } else {
+    const cuuint64_t N = (cuuint64_t)(key_side ? s.lay.Nk : s.lay.Nq);
+    dims[0] = d;
+    dims[1] = N;
+    dims[2] = (cuuint64_t)s.B * s.H;
+    strides[0] = d * 2;
+    strides[1] = N * d * 2;
+    box[0] = 64;
+    box[1] = (cuuint32_t)box_rows;
+    box[2] = 1;
+  }
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, s.bf16() ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 // Dropout probability -> generator parameters: t = round(p * 65536), keep
 // scale 65536 / (65536 - t).  False for p outside [0, 1) (NaN included) or
@@ -110,24 +164,22 @@ fa_status check_block_mask(const uint8_t* block_mask, int mask_heads, int B, int
   return FA_OK;
 }
 
-fa_status forward_impl(const void* q, const void* k, const void* v, void* o, float* lse, const uint8_t* block_mask,
-                       int mask_heads, int B, int H, int N, int d, int dtype, int causal, float scale,
-                       void* stream, const fa::DropParams* drop = nullptr) {
-  fa_status st = check_shape(B, H, N, d, dtype);
+// ---------------------------------------------------------------- runners
+fa_status run_forward(const Shape& s, const void* q, const void* k, const void* v, void* o, float* lse,
+                      const uint8_t* block_mask, int mask_heads, int causal, float scale, void* stream,
+                      const fa::DropParams* drop) {
+  fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
-  const bool bf16 = dtype == FA_BF16;
   fa::FwdArgs a;
-  const int BH = B * H;
-  if (!make_map(&a.tm_q, q, bf16, d, N, BH, 128) || !make_map(&a.tm_k, k, bf16, d, N, BH, 128) ||
-      !make_map(&a.tm_v, v, bf16, d, N, BH, 128))
+  if (!make_map(&a.tm_q, q, s, false, 128) || !make_map(&a.tm_k, k, s, true, 128) ||
+      !make_map(&a.tm_v, v, s, true, 128))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;
-  a.N = N;
-  a.BH = BH;
+  a.lay = s.lay;
+  a.BH = s.B * s.H;
   a.scale_log2 = scale * kLog2e;
   a.block_mask = block_mask;
   a.mask_heads = mask_heads;
@@ -136,75 +188,42 @@ fa_status forward_impl(const void* q, const void* k, const void* v, void* o, flo
   // p rounding to 0 drops nothing: the plain kernel computes exactly that.
   a.dropout = drop != nullptr && drop->t > 0;
   if (a.dropout) a.drop = *drop;
-  const cudaError_t e = a.dropout ? fa::launch_forward_dropout(d, causal != 0, bf16, a, static_cast<cudaStream_t>(stream))
-                                  : fa::launch_forward(d, causal != 0, bf16, a, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = s.varlen()  ? fa::launch_forward_varlen(s.width(), causal != 0, s.bf16(), a, cs)
+                        : a.dropout ? fa::launch_forward_dropout(s.width(), causal != 0, s.bf16(), a, cs)
+                                    : fa::launch_forward(s.width(), causal != 0, s.bf16(), a, cs);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                     int d, int dtype, int causal, float scale, void* stream) {
-  return forward_impl(q, k, v, o, lse, nullptr, 1, B, H, N, d, dtype, causal, scale, stream);
-}
-
-fa_status fa_forward_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
-                                 const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d, int dtype,
-                                 int causal, float scale, void* stream) {
-  const fa_status st = check_block_mask(block_mask, mask_heads, B, H);
-  if (st != FA_OK) return st;
-  return forward_impl(q, k, v, o, lse, block_mask, mask_heads, B, H, N, d, dtype, causal, scale, stream);
-}
-
-size_t fa_backward_workspace_size(int B, int H, int N, int d) {
-  if (check_shape(B, H, N, d, FA_BF16) != FA_OK) return 0;
-  const size_t rows = (size_t)B * H * N;
-  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
-}
-
-fa_status fa_backward_preprocess(const void* o, const void* dO, float* delta, float* dq_accum, int B, int H,
-                                 int N, int d, int dtype, void* stream) {
-  fa_status st = check_shape(B, H, N, d, dtype);
-  if (st != FA_OK) return st;
+fa_status run_preprocess(const Shape& s, const void* o, const void* dO, float* delta, float* dq_accum,
+                         void* stream) {
   if (!aligned16(o) || !aligned16(dO) || !aligned16(delta) || !aligned16(dq_accum)) return FA_ERR_INVALID_ARG;
-  const long long rows = (long long)B * H * N;
-  if (fa::launch_backward_preprocess(d, dtype == FA_BF16, o, dO, delta, dq_accum, rows,
+  if (fa::launch_backward_preprocess(s.d, s.bf16(), o, dO, delta, dq_accum, s.q_rows(),
                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }
 
-}  // extern "C"
-
-namespace {
-
-fa_status dkdv_impl(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* delta,
-                    float* dq_accum, void* dk, void* dv, const uint8_t* block_mask, int mask_heads, int B, int H,
-                    int N, int d, int dtype, int causal, float scale, void* stream,
-                    const fa::DropParams* drop = nullptr) {
-  fa_status st = check_shape(B, H, N, d, dtype);
+fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                   const float* delta, float* dq_accum, void* dk, void* dv, const uint8_t* block_mask,
+                   int mask_heads, int causal, float scale, void* stream, const fa::DropParams* drop) {
+  fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(delta) || !aligned16(dq_accum) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
-  const bool bf16 = dtype == FA_BF16;
-  const int BH = B * H;
-  const int bq = fa::backward_q_tile(d);
+  const int bq = fa::backward_q_tile(s.width());
   fa::BwdArgs a;
-  if (!make_map(&a.tm_q, q, bf16, d, N, BH, bq) || !make_map(&a.tm_do, dO, bf16, d, N, BH, bq) ||
-      !make_map(&a.tm_k, k, bf16, d, N, BH, 128) || !make_map(&a.tm_v, v, bf16, d, N, BH, 128))
+  if (!make_map(&a.tm_q, q, s, false, bq) || !make_map(&a.tm_do, dO, s, false, bq) ||
+      !make_map(&a.tm_k, k, s, true, 128) || !make_map(&a.tm_v, v, s, true, 128))
     return FA_ERR_CUDA;
   a.dk = dk;
   a.dv = dv;
   a.lse = lse;
   a.delta = delta;
   a.dq_accum = dq_accum;
-  a.N = N;
-  a.BH = BH;
+  a.lay = s.lay;
+  a.BH = s.B * s.H;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
   a.block_mask = block_mask;
@@ -213,92 +232,237 @@ fa_status dkdv_impl(const void* q, const void* k, const void* v, const void* dO,
   if (!a.status) return FA_ERR_CUDA;
   a.dropout = drop != nullptr && drop->t > 0;
   if (a.dropout) a.drop = *drop;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = a.dropout ? fa::launch_backward_dkdv_dropout(d, causal != 0, bf16, a, s)
-                                  : fa::launch_backward_dkdv(d, causal != 0, bf16, a, s);
-  if (e != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = s.varlen()  ? fa::launch_backward_dkdv_varlen(s.width(), causal != 0, s.bf16(), a, cs)
+                        : a.dropout ? fa::launch_backward_dkdv_dropout(s.width(), causal != 0, s.bf16(), a, cs)
+                                    : fa::launch_backward_dkdv(s.width(), causal != 0, s.bf16(), a, cs);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                           const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N, int d,
-                           int dtype, int causal, float scale, void* stream) {
-  return dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, B, H, N, d, dtype, causal, scale, stream);
-}
-
-fa_status fa_backward_dkdv_blocksparse(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                                       const float* delta, float* dq_accum, void* dk, void* dv,
-                                       const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d,
-                                       int dtype, int causal, float scale, void* stream) {
-  const fa_status st = check_block_mask(block_mask, mask_heads, B, H);
+fa_status run_convert(const Shape& s, const float* dq_accum, void* dq, float scale, void* stream) {
+  fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  return dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, B, H, N, d, dtype, causal,
-                   scale, stream);
-}
-
-fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,
-                                 float scale, void* stream) {
-  fa_status st = check_shape(B, H, N, d, dtype);
-  if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
   if (!aligned16(dq_accum) || !aligned16(dq)) return FA_ERR_INVALID_ARG;
-  const long long rows = (long long)B * H * N;
-  if (fa::launch_backward_dq_convert(d, dtype == FA_BF16, dq_accum, dq, rows, scale,
+  if (fa::launch_backward_dq_convert(s.d, s.bf16(), dq_accum, dq, s.q_rows(), scale,
                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }
 
-}  // extern "C"
+size_t workspace_bytes_for(const Shape& s) {
+  const size_t rows = (size_t)s.q_rows();
+  return align256(rows * sizeof(float)) + align256(rows * s.d * sizeof(float));
+}
 
-namespace {
-
-fa_status backward_impl(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                        void* dq, void* dk, void* dv, const uint8_t* block_mask, int mask_heads, int B, int H, int N,
-                        int d, int dtype, int causal, float scale, void* workspace, size_t workspace_bytes,
-                        void* stream, const fa::DropParams* drop = nullptr) {
-  fa_status st = check_shape(B, H, N, d, dtype);
+fa_status run_backward(const Shape& s, const void* q, const void* k, const void* v, const void* o, const void* dO,
+                       const float* lse, void* dq, void* dk, void* dv, const uint8_t* block_mask, int mask_heads,
+                       int causal, float scale, void* workspace, size_t workspace_bytes, void* stream,
+                       const fa::DropParams* drop) {
+  fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
-  const size_t need = fa_backward_workspace_size(B, H, N, d);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < workspace_bytes_for(s))
     return FA_ERR_WORKSPACE;
-  const size_t rows = (size_t)B * H * N;
   float* delta = static_cast<float*>(workspace);
-  float* dq_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(float)));
-  if ((st = fa_backward_preprocess(o, dO, delta, dq_accum, B, H, N, d, dtype, stream)) != FA_OK) return st;
-  if ((st = dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, B, H, N, d, dtype, causal,
-                      scale, stream, drop)) != FA_OK)
+  float* dq_accum =
+      reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)s.q_rows() * sizeof(float)));
+  if ((st = run_preprocess(s, o, dO, delta, dq_accum, stream)) != FA_OK) return st;
+  if ((st = run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, causal, scale, stream,
+                     drop)) != FA_OK)
     return st;
-  return fa_backward_dq_convert(dq_accum, dq, B, H, N, d, dtype, scale, stream);
+  return run_convert(s, dq_accum, dq, scale, stream);
 }
 
 }  // namespace
 
+// ---------------------------------------------------------------- entry points
 extern "C" {
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null/misaligned pointer, bad size or bad scale";
+    case FA_ERR_UNSUPPORTED:
+      return "FA_ERR_UNSUPPORTED: head dim must be 64, 96 or 128, dtype fp16/bf16, rows*H*d < 2^31";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA launch or the stream failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up waiting on its pipeline";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case FA_ERR_SCRATCH_TOO_SMALL:
+      return "FA_ERR_SCRATCH_TOO_SMALL: fa_backward_noalloc needs more than its fixed 32 MiB scratch; use fa_backward";
+    case FA_ERR_SEQLENS:
+      return "FA_ERR_SEQLENS: a cu_seqlens range exceeded the packed totals or the maximum lengths; it was skipped";
+    default: return "unknown fa_status";
+  }
+}
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                     int d, int dtype, int causal, float scale, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_forward(s, q, k, v, o, lse, nullptr, 1, causal, scale, stream, nullptr);
+}
+
+fa_status fa_forward_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d, int dtype,
+                                 int causal, float scale, void* stream) {
+  Shape s;
+  fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_block_mask(block_mask, mask_heads, B, H)) != FA_OK) return st;
+  return run_forward(s, q, k, v, o, lse, block_mask, mask_heads, causal, scale, stream, nullptr);
+}
+
+fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                             int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                             uint32_t offset, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return run_forward(s, q, k, v, o, lse, nullptr, 1, causal, scale, stream, &dp);
+}
+
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                            const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k, int total_q,
+                            int total_k, int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                            uint32_t offset, void* stream) {
+  Shape s;
+  const fa_status st = varlen_shape(cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, max_seqlen_k, total_q, total_k,
+                                    d, dtype, &s);
+  if (st != FA_OK) return st;
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return run_forward(s, q, k, v, o, lse, nullptr, 1, causal, scale, stream, &dp);
+}
+
+size_t fa_backward_workspace_size(int B, int H, int N, int d) {
+  Shape s;
+  if (dense_shape(B, H, N, N, d, FA_BF16, &s) != FA_OK) return 0;
+  return workspace_bytes_for(s);
+}
+
+size_t fa_backward_varlen_workspace_size(int total_q, int H, int d) {
+  if (total_q < 1 || H < 1 || check_dims(d, FA_BF16) != FA_OK) return 0;
+  if ((long long)total_q * H * d >= (1LL << 31)) return 0;
+  const size_t rows = (size_t)total_q * H;
+  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+}
 
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, const void* dO,
                       const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int dtype,
                       int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
-  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, nullptr, 1, B, H, N, d, dtype, causal, scale, workspace,
-                       workspace_bytes, stream);
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_backward(s, q, k, v, o, dO, lse, dq, dk, dv, nullptr, 1, causal, scale, workspace, workspace_bytes,
+                      stream, nullptr);
 }
 
 fa_status fa_backward_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                   const float* lse, void* dq, void* dk, void* dv, const uint8_t* block_mask,
                                   int mask_heads, int B, int H, int N, int d, int dtype, int causal, float scale,
                                   void* workspace, size_t workspace_bytes, void* stream) {
-  const fa_status st = check_block_mask(block_mask, mask_heads, B, H);
+  Shape s;
+  fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
   if (st != FA_OK) return st;
-  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, block_mask, mask_heads, B, H, N, d, dtype, causal, scale,
-                       workspace, workspace_bytes, stream);
+  if ((st = check_block_mask(block_mask, mask_heads, B, H)) != FA_OK) return st;
+  return run_backward(s, q, k, v, o, dO, lse, dq, dk, dv, block_mask, mask_heads, causal, scale, workspace,
+                      workspace_bytes, stream, nullptr);
 }
 
+fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int dtype,
+                              int causal, float scale, float p_drop, uint64_t seed, uint32_t offset, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return run_backward(s, q, k, v, o, dO, lse, dq, dk, dv, nullptr, 1, causal, scale, workspace, workspace_bytes,
+                      stream, &dp);
+}
+
+fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                             const float* lse, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                             const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k, int total_q,
+                             int total_k, int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                             uint32_t offset, void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  const fa_status st = varlen_shape(cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, max_seqlen_k, total_q, total_k,
+                                    d, dtype, &s);
+  if (st != FA_OK) return st;
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return run_backward(s, q, k, v, o, dO, lse, dq, dk, dv, nullptr, 1, causal, scale, workspace, workspace_bytes,
+                      stream, &dp);
+}
+
+fa_status fa_backward_preprocess(const void* o, const void* dO, float* delta, float* dq_accum, int B, int H,
+                                 int N, int d, int dtype, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_preprocess(s, o, dO, delta, dq_accum, stream);
+}
+
+fa_status fa_backward_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                           const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N, int d,
+                           int dtype, int causal, float scale, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, causal, scale, stream, nullptr);
+}
+
+fa_status fa_backward_dkdv_blocksparse(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                       const float* delta, float* dq_accum, void* dk, void* dv,
+                                       const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d,
+                                       int dtype, int causal, float scale, void* stream) {
+  Shape s;
+  fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_block_mask(block_mask, mask_heads, B, H)) != FA_OK) return st;
+  return run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, causal, scale, stream,
+                  nullptr);
+}
+
+fa_status fa_backward_dkdv_dropout(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                   const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N,
+                                   int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                                   uint32_t offset, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, causal, scale, stream, &dp);
+}
+
+fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,
+                                 float scale, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_convert(s, dq_accum, dq, scale, stream);
+}
+
+fa_status fa_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, float p_drop, uint64_t seed, uint32_t offset,
+                               void* stream) {
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  if (BH < 1 || Nq < 1 || Nk < 1 || !keep) return FA_ERR_INVALID_ARG;
+  if (fa::launch_dropout_keep_mask(keep, BH, Nq, Nk, dp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- decoding
 namespace {
+
 fa_status decode_plan(int B, int H, int Nq, int Nk, int d, int num_splits, int* splits, int* chunk,
                       size_t* bytes) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
@@ -315,7 +479,10 @@ fa_status decode_plan(int B, int H, int Nq, int Nk, int d, int num_splits, int* 
   *bytes = align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
   return FA_OK;
 }
+
 }  // namespace
+
+extern "C" {
 
 size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
   int s, c;
@@ -358,44 +525,6 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o
   return FA_OK;
 }
 
-fa_status fa_forward_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                             int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
-                             uint32_t offset, void* stream) {
-  fa::DropParams dp;
-  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
-  return forward_impl(q, k, v, o, lse, nullptr, 1, B, H, N, d, dtype, causal, scale, stream, &dp);
-}
-
-fa_status fa_backward_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int dtype,
-                              int causal, float scale, float p_drop, uint64_t seed, uint32_t offset, void* workspace,
-                              size_t workspace_bytes, void* stream) {
-  fa::DropParams dp;
-  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
-  return backward_impl(q, k, v, o, dO, lse, dq, dk, dv, nullptr, 1, B, H, N, d, dtype, causal, scale, workspace,
-                       workspace_bytes, stream, &dp);
-}
-
-fa_status fa_backward_dkdv_dropout(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-                                   const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N,
-                                   int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
-                                   uint32_t offset, void* stream) {
-  fa::DropParams dp;
-  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
-  return dkdv_impl(q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, B, H, N, d, dtype, causal, scale, stream,
-                   &dp);
-}
-
-fa_status fa_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, float p_drop, uint64_t seed, uint32_t offset,
-                               void* stream) {
-  fa::DropParams dp;
-  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
-  if (BH < 1 || Nq < 1 || Nk < 1 || !keep) return FA_ERR_INVALID_ARG;
-  if (fa::launch_dropout_keep_mask(keep, BH, Nq, Nk, dp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FA_ERR_CUDA;
-  return FA_OK;
-}
-
 fa_status fa_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   unsigned int v = 0;
@@ -404,6 +533,7 @@ fa_status fa_device_status(void* stream) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
     if (v & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
+    if (v & fa::kStatusBadSeqlens) return FA_ERR_SEQLENS;
   }
   return FA_OK;
 }

@@ -10,8 +10,8 @@ namespace {
 
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_dkdv_s(const BwdArgs& a, cudaStream_t stream) {
-  return a.block_mask ? launch_dkdv_t<D, CAUSAL, BF16, true, false>(a, stream)
-                      : launch_dkdv_t<D, CAUSAL, BF16, false, false>(a, stream);
+  return a.block_mask ? launch_dkdv_t<D, CAUSAL, BF16, true, false, false>(a, stream)
+                      : launch_dkdv_t<D, CAUSAL, BF16, false, false, false>(a, stream);
 }
 
 }  // namespace

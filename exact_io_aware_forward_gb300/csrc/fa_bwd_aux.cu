@@ -46,13 +46,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// One row is handled by D/8 consecutive threads, 8 elements (16 bytes) each.
+// One row is handled by TPR consecutive threads (a power of two), VPT
+// 16-byte vectors (8 elements) each: D = 64: 8 x 1, 96: 4 x 3, 128: 16 x 1.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __restrict__ o,
                                                                 const uint4* __restrict__ dO,
                                                                 float* __restrict__ delta,
                                                                 float4* __restrict__ dq_accum, long long rows) {
-  constexpr int TPR = D / 8;
+  constexpr int TPR = D == 96 ? 4 : D / 8;
+  constexpr int VPT = D / 8 / TPR;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const int part = threadIdx.x % TPR;
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -62,19 +64,25 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
        (t - (threadIdx.x & 31)) / TPR < rows; t += stride) {
     const long long row = t / TPR;
     const bool active = row < rows;
-    const long long idx = active ? t : 0;
-    float a[8], b[8];
-    unpack8<BF16>(o[idx], a);
-    unpack8<BF16>(dO[idx], b);
+    const long long idx0 = active ? row * (D / 8) + part * VPT : 0;  // first 16-byte vector
     float acc = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+    for (int u = 0; u < VPT; ++u) {
+      float a[8], b[8];
+      unpack8<BF16>(o[idx0 + u], a);
+      unpack8<BF16>(dO[idx0 + u], b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+    }
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
     if (active) {
       if (part == 0) delta[row] = acc;
-      dq_accum[2 * idx] = zero;
-      dq_accum[2 * idx + 1] = zero;
+#pragma unroll
+      for (int u = 0; u < VPT; ++u) {
+        dq_accum[2 * (idx0 + u)] = zero;
+        dq_accum[2 * (idx0 + u) + 1] = zero;
+      }
     }
   }
 }
@@ -109,13 +117,15 @@ int grid_for(long long threads_needed) {
 
 cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const void* dO, float* delta,
                                        float* dq_accum, long long rows, cudaStream_t stream) {
-  const long long threads = rows * (d / 8);
+  const long long threads = rows * (d == 96 ? 4 : d / 8);
   const int grid = grid_for(threads);
   const uint4* o4 = static_cast<const uint4*>(o);
   const uint4* d4 = static_cast<const uint4*>(dO);
   float4* acc = reinterpret_cast<float4*>(dq_accum);
   if (d == 64 && bf16) fa_bwd_preprocess_kernel<64, true><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else if (d == 64) fa_bwd_preprocess_kernel<64, false><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
+  else if (d == 96 && bf16) fa_bwd_preprocess_kernel<96, true><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
+  else if (d == 96) fa_bwd_preprocess_kernel<96, false><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else if (d == 128 && bf16) fa_bwd_preprocess_kernel<128, true><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else if (d == 128) fa_bwd_preprocess_kernel<128, false><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else return cudaErrorInvalidValue;

@@ -27,7 +27,7 @@ __global__ void fa_dropout_keep_mask_kernel(uint8_t* __restrict__ keep, int BH, 
 
 cudaError_t launch_backward_dkdv_dropout(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream) {
 #define FA_BWD_CASE(DD, CC, BB) \
-  if (d == DD && causal == CC && bf16 == BB) return launch_dkdv_t<DD, CC, BB, false, true>(a, stream);
+  if (d == DD && causal == CC && bf16 == BB) return launch_dkdv_t<DD, CC, BB, false, true, false>(a, stream);
   FA_BWD_CASE(64, false, false)
   FA_BWD_CASE(64, false, true)
   FA_BWD_CASE(64, true, false)

@@ -57,6 +57,7 @@
 #include <cuda_fp16.h>
 
 #include "fa_internal.h"
+#include "fa_layout.cuh"
 #include "fa_philox.cuh"
 #include "fa_ptx.cuh"
 
@@ -142,12 +143,14 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
                : "memory");
 }
 
-// Thread-owned row of a [rows, D] 16-bit tensor, written from TMEM columns
-// [taddr, taddr + D) times `mul` (skipped when `valid` is false).
+// Thread-owned row of a [rows, dh] 16-bit tensor, written from TMEM columns
+// [taddr, taddr + dh) times `mul` (skipped when `valid` is false); dh <= D is
+// a multiple of 32.
 template <int D, bool BF16>
-__device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint4* dst, bool valid, float mul) {
+__device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint4* dst, bool valid, float mul, int dh) {
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
+    if (32 * c >= dh) break;
     float v[32];
     tmem_ld32(taddr + 32 * c, v);
     tmem_ld_wait(v);
@@ -170,12 +173,12 @@ __device__ __forceinline__ uint32_t transpose8_step(uint32_t x, int lane, int m,
   return (lane & m) ? ((x & hi_mask) | ((y & hi_mask) >> m)) : ((x & lo_mask) | ((y & lo_mask) << m));
 }
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(640, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        void* __restrict__ dk, void* __restrict__ dv, const float* __restrict__ lse,
-                       const float* __restrict__ delta, float* __restrict__ dq_accum, int N, int BH,
+                       const float* __restrict__ delta, float* __restrict__ dq_accum, SeqLayout lay, int BH,
                        float scale, float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads,
                        DropParams drop, unsigned int* status) {
   using C = BwdCfg<D>;
@@ -211,12 +214,19 @@ __global__ void __launch_bounds__(640, 1)
   // Head-major order: the CTAs of one head run together, so its Q, dO and
   // float32 dQ accumulator stay in L2; within a head key tile 0 (which sees
   // every query tile under the causal mask) goes first.
-  const int n_kvt = (N + C::BKV - 1) / C::BKV;
+  const int n_kvt = (lay.Nk + C::BKV - 1) / C::BKV;  // key tiles of the longest sequence
   const int bh = blockIdx.x / n_kvt;
   const int j = blockIdx.x % n_kvt;
   const int kv0 = j * C::BKV;
-  const int n_q = (N + BQ - 1) / BQ;
-  const int i_begin = CAUSAL ? kv0 / BQ : 0;
+  const SeqView sv = seq_view<VARLEN>(lay, bh);
+  if (!sv.ok && kv0 == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSeqlens);
+  if (kv0 >= sv.nk) return;  // past the end of a shorter (or rejected) sequence: the whole CTA leaves
+  const int Nq = sv.nq, Nk = sv.nk;
+  const int off = Nk - Nq;  // causal: key visible iff key <= query + off
+  const int dh = lay.dh;
+  const int n_q = (Nq + BQ - 1) / BQ;
+  // Causal: the first query that sees key kv0 is kv0 - off.
+  const int i_begin = CAUSAL ? (kv0 - off <= 0 ? 0 : (kv0 - off) / BQ) : 0;
   // Query tiles this key tile meets: [i_begin, n_q), and under a block mask
   // only those whose 128-row query block keeps key tile j.  Every role walks
   // the same sequence; `it` counts the tiles visited.
@@ -230,9 +240,8 @@ __global__ void __launch_bounds__(640, 1)
   if (SPARSE) {
     for (int i = next_tile(i_begin); i < n_q; i = next_tile(i + 1)) ++n_it;
   } else {
-    n_it = n_q - i_begin;
+    n_it = n_q > i_begin ? n_q - i_begin : 0;
   }
-  const long long head_row = (long long)bh * N;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -275,9 +284,10 @@ __global__ void __launch_bounds__(640, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
+      const int2 ck = sv.kcoord(kv0);
       for (int s = 0; s < C::SLABS; ++s) {
-        tma_load_3d(sK + s * C::KV_SLAB, &tm_k, kv_full, s * 64, kv0, bh);
-        tma_load_3d(sV + s * C::KV_SLAB, &tm_v, kv_full, s * 64, kv0, bh);
+        tma_load_3d(sK + s * C::KV_SLAB, &tm_k, kv_full, s * 64, ck.x, ck.y);
+        tma_load_3d(sV + s * C::KV_SLAB, &tm_v, kv_full, s * 64, ck.x, ck.y);
       }
       int issued = 0;
       for (int it = 0, i = next_tile(i_begin); it < n_it; ++it, i = next_tile(i + 1)) {
@@ -285,10 +295,10 @@ __global__ void __launch_bounds__(640, 1)
         const uint32_t use = (uint32_t)(it / C::QS);
         if (!mbar_wait(&q_empty[b], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         mbar_arrive_expect_tx(&q_full[b], 2 * C::Q_TILE);
-        const int q0 = i * BQ;
+        const int2 cq = sv.qcoord(i * BQ);
         for (int s = 0; s < C::SLABS; ++s) {
-          tma_load_3d(sQ + b * C::Q_TILE + s * C::Q_SLAB, &tm_q, &q_full[b], s * 64, q0, bh);
-          tma_load_3d(sDO + b * C::Q_TILE + s * C::Q_SLAB, &tm_do, &q_full[b], s * 64, q0, bh);
+          tma_load_3d(sQ + b * C::Q_TILE + s * C::Q_SLAB, &tm_q, &q_full[b], s * 64, cq.x, cq.y);
+          tma_load_3d(sDO + b * C::Q_TILE + s * C::Q_SLAB, &tm_do, &q_full[b], s * 64, cq.x, cq.y);
         }
         issued = it + 1;
       }
@@ -412,6 +422,8 @@ __global__ void __launch_bounds__(640, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int key = kv0 + r;
+    const int key_rel = key - off;  // causal: masked iff key_rel > query
+    const int kv0_rel = kv0 - off;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
     // Per query column: -LSE*log2(e) (so that P = exp2(s*scale*log2e - LSE*log2e))
@@ -420,10 +432,10 @@ __global__ void __launch_bounds__(640, 1)
     auto fetch = [&](int i) {  // query tile i
       const int q = i * BQ + h * CW + r;
       if (r < CW) {
-        if (q < N) {
-          const float lq = lse[head_row + q];
+        if (q < Nq) {
+          const float lq = lse[sv.qflat(q)];
           pre_l = lq == -pos_inf() ? -pos_inf() : -lq * kLog2e;  // a row with no visible key: P = 0
-          pre_d = -delta[head_row + q];
+          pre_d = -delta[sv.qflat(q)];
         } else {  // padding query: P = exp2(-inf) = 0
           pre_l = -pos_inf();
           pre_d = 0.f;
@@ -492,7 +504,7 @@ __global__ void __launch_bounds__(640, 1)
           if (lane == 0) mbar_arrive(sdp_empty);
         }
         const int c0 = q0 + col;  // first query of this sub-chunk
-        const bool need_mask = (CAUSAL && c0 < kv0 + C::BKV - 1) || (kv0 + C::BKV > N);
+        const bool need_mask = (CAUSAL && c0 < kv0_rel + C::BKV - 1) || (kv0 + C::BKV > Nk);
         const uint32_t keep = DROP ? (((sc >> 1) ? kw1 : kw0) >> (16 * (sc & 1))) : 0xffffu;  // bit c: (c0 + c, key) kept
         uint32_t pp[8], dd[8];
 #pragma unroll
@@ -505,8 +517,8 @@ __global__ void __launch_bounds__(640, 1)
           float p0 = ex2_approx(x0);
           float p1 = ex2_approx(x1);
           if (need_mask) {
-            if (key >= N || (CAUSAL && key > c0 + c)) p0 = 0.f;
-            if (key >= N || (CAUSAL && key > c0 + c + 1)) p1 = 0.f;
+            if (key >= Nk || (CAUSAL && key_rel > c0 + c)) p0 = 0.f;
+            if (key >= Nk || (CAUSAL && key_rel > c0 + c + 1)) p1 = 0.f;
           }
           float dp0 = dp[c], dp1 = dp[c + 1];
           float pv0 = p0, pv1 = p1;  // dV operand: the kept P
@@ -553,11 +565,11 @@ __global__ void __launch_bounds__(640, 1)
       if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
       if (ok) {
         tc_fence_after();
-        uint4* dst = reinterpret_cast<uint4*>(dv) + (head_row + key) * (D / 8);
+        uint4* dst = reinterpret_cast<uint4*>(dv) + sv.kflat(key) * (dh / 8);
         if (n_it > 0) {
-          store_rows_from_tmem<D, BF16>(lane_base + C::COL_DV, dst, key < N, DROP ? drop.keep_scale : 1.f);
-        } else if (key < N) {  // no query tile kept this key tile (block-sparse): dV = 0
-          for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+          store_rows_from_tmem<D, BF16>(lane_base + C::COL_DV, dst, key < Nk, DROP ? drop.keep_scale : 1.f, dh);
+        } else if (key < Nk) {  // no query sees this key tile (block mask, or causal with Nq < Nk): dV = 0
+          for (int q = 0; q < dh / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     }
@@ -582,13 +594,20 @@ __global__ void __launch_bounds__(640, 1)
       if (lane == 0) mbar_arrive(&dq_empty[b]);
       const int q0 = i * BQ;
       if (C::DQT) {  // lane = feature r, column = query q0 + 32g + c: one 128-byte line per warp and column
-        float* base = dq_accum + (head_row + q0 + 32 * g) * D + r;
+        float* base = dq_accum + sv.qflat(q0 + 32 * g) * dh + r;
+        if (!sv.varlen && dh == D) {  // dense rows D floats apart: constant offsets
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (q0 + 32 * g + c < N) red_add_f32(base + (long long)c * D, v[c]);
-      } else {  // lane = query q0 + r, column = feature 32g + c
-        if (q0 + r < N) {
-          float* base = dq_accum + (head_row + q0 + r) * D + 32 * g;
+          for (int c = 0; c < 32; ++c)
+            if (q0 + 32 * g + c < Nq) red_add_f32(base + c * D, v[c]);
+        } else if (r < dh) {
+          const long long step = (long long)sv.rstride * dh;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (q0 + 32 * g + c < Nq) red_add_f32(base + c * step, v[c]);
+        }
+      } else {  // lane = query q0 + r, column = feature 32g + c (dh = D = 64)
+        if (q0 + r < Nq) {
+          float* base = dq_accum + sv.qflat(q0 + r) * dh + 32 * g;
 #pragma unroll
           for (int c = 0; c < 32; c += 4) red_add_v4(base + c, v[c], v[c + 1], v[c + 2], v[c + 3]);
         }
@@ -599,11 +618,11 @@ __global__ void __launch_bounds__(640, 1)
       if (ok) {
         tc_fence_after();
         const int key = kv0 + r;
-        uint4* dst = reinterpret_cast<uint4*>(dk) + (head_row + key) * (D / 8);
+        uint4* dst = reinterpret_cast<uint4*>(dk) + sv.kflat(key) * (dh / 8);
         if (n_it > 0) {
-          store_rows_from_tmem<D, BF16>(lane_base + C::COL_DK, dst, key < N, scale);
-        } else if (key < N) {  // dK = 0 likewise
-          for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+          store_rows_from_tmem<D, BF16>(lane_base + C::COL_DK, dst, key < Nk, scale, dh);
+        } else if (key < Nk) {  // dK = 0 likewise
+          for (int q = 0; q < dh / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     }
@@ -617,17 +636,17 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, BF16, SPARSE, DROP>;
+  auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, BF16, SPARSE, DROP, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int n_kv = (a.N + C::BKV - 1) / C::BKV;
+  const int n_kv = (a.lay.Nk + C::BKV - 1) / C::BKV;
   const long long grid = (long long)n_kv * a.BH;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dk, a.dv, a.lse,
-                                                         a.delta, a.dq_accum, a.N, a.BH, a.scale, a.scale_log2,
+                                                         a.delta, a.dq_accum, a.lay, a.BH, a.scale, a.scale_log2,
                                                          a.block_mask, a.mask_heads, a.drop, a.status);
   return cudaGetLastError();
 }

@@ -7,7 +7,7 @@ namespace fa {
 
 cudaError_t launch_forward_dropout(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream) {
 #define FA_FWD_CASE(DD, CC, BB) \
-  if (d == DD && causal == CC && bf16 == BB) return launch_fwd_t<DD, CC, BB, false, true>(a, stream);
+  if (d == DD && causal == CC && bf16 == BB) return launch_fwd_t<DD, CC, BB, false, true, false>(a, stream);
   FA_FWD_CASE(64, false, false)
   FA_FWD_CASE(64, false, true)
   FA_FWD_CASE(64, true, false)

@@ -36,7 +36,10 @@
 //
 // Causal: key tiles entirely above the diagonal are never loaded or
 // multiplied (section 4.5's whole-block skip); the diagonal tile and the
-// ragged tail (keys >= N) are masked elementwise to -inf.
+// ragged tail (keys >= N) are masked elementwise to -inf.  With Nq != Nk the
+// diagonal is bottom-right aligned (query i sits at position i + Nk - Nq); a
+// row that sees no key gets O = 0 and LSE = -inf.  Packed variable-length
+// batches (SeqLayout) give every CTA its own sequence lengths and row bases.
 // Block-sparse (SPARSE): the same skip driven by a mask of 128 x 128 blocks
 // (section 06 generalises the whole-block skip to any pattern); a query tile
 // that keeps no key tile writes O = 0 and LSE = -inf.
@@ -50,6 +53,7 @@
 #include <cuda_fp16.h>
 
 #include "fa_internal.h"
+#include "fa_layout.cuh"
 #include "fa_philox.cuh"
 #include "fa_ptx.cuh"
 
@@ -122,11 +126,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o,
-                  float* __restrict__ lse, int N, int BH, int n_qblocks, float scale_log2,
+                  float* __restrict__ lse, SeqLayout lay, int BH, int n_qblocks, float scale_log2,
                   const uint8_t* __restrict__ block_mask, int mask_heads, DropParams drop,
                   unsigned int* status) {
   using C = FwdCfg<D>;
@@ -152,9 +156,16 @@ __global__ void __launch_bounds__(384, 1)
   const int bh = blockIdx.x % BH;
   const int qb = n_qblocks - 1 - blockIdx.x / BH;
   const int q0 = qb * (C::QT * C::BM);
-  const int n_kv = (N + C::BN - 1) / C::BN;
-  const int n0 = CAUSAL ? min(n_kv, q0 / C::BN + 1) : n_kv;  // key tiles seen by query tile 0
-  const int n1 = CAUSAL ? min(n_kv, q0 / C::BN + 2) : n_kv;  // ... and by query tile 1
+  const SeqView sv = seq_view<VARLEN>(lay, bh);
+  if (!sv.ok && q0 == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSeqlens);
+  if (q0 >= sv.nq) return;  // past the end of a shorter (or rejected) sequence: the whole CTA leaves
+  const int Nq = sv.nq, Nk = sv.nk;
+  const int off = Nk - Nq;  // causal: key visible iff key <= row + off
+  const int dh = lay.dh;
+  const int n_kv = (Nk + C::BN - 1) / C::BN;
+  // key tiles seen by query tile 0, and by query tile 1 (n1 >= n0)
+  const int n0 = CAUSAL ? causal_key_tiles(q0 + C::BM - 1, off, n_kv, C::BN) : n_kv;
+  const int n1 = CAUSAL ? causal_key_tiles(q0 + 2 * C::BM - 1, off, n_kv, C::BN) : n_kv;
   // Block-sparse: one mask byte per (128-row query tile, 128-key tile); a key
   // tile is loaded only if one of the two query tiles keeps it.
   const uint8_t* mrow0 = nullptr;
@@ -209,9 +220,10 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       int issued = 0;  // K/V tiles whose copy has been started
       mbar_arrive_expect_tx(q_full, C::QT * C::TILE);
-      for (int t = 0; t < C::QT; ++t)
-        for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sQ + t * C::TILE + s * C::SLAB, &tm_q, q_full, s * 64, q0 + t * C::BM, bh);
+      for (int t = 0; t < C::QT; ++t) {
+        const int2 c = sv.qcoord(q0 + t * C::BM);
+        for (int s = 0; s < C::SLABS; ++s) tma_load_3d(sQ + t * C::TILE + s * C::SLAB, &tm_q, q_full, s * 64, c.x, c.y);
+      }
       if constexpr (!SPARSE) {
         for (int u = 0; u < 2 * n1; ++u) {  // K_0, V_0, K_1, V_1, ...
           const int slot = u % C::NS;
@@ -219,8 +231,9 @@ __global__ void __launch_bounds__(384, 1)
           if (!mbar_wait(&ring_empty[slot], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
           mbar_arrive_expect_tx(&ring_full[slot], C::TILE);
           const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
+          const int2 c = sv.kcoord((u >> 1) * C::BN);
           for (int s = 0; s < C::SLABS; ++s)
-            tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, (u >> 1) * C::BN, bh);
+            tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, c.x, c.y);
           issued = u + 1;
         }
       } else {
@@ -234,8 +247,9 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = mbar_wait(&ring_empty[slot], (use & 1) ^ 1, abort_flag, status, kStatusTimeout))) break;
             mbar_arrive_expect_tx(&ring_full[slot], C::TILE);
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
+            const int2 c = sv.kcoord(j * C::BN);
             for (int s = 0; s < C::SLABS; ++s)
-              tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, j * C::BN, bh);
+              tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, c.x, c.y);
             issued = uu + 1;
           }
           ++u;
@@ -301,7 +315,7 @@ __global__ void __launch_bounds__(384, 1)
           mma_commit(&s_full[1]);
           mma_commit(&ring_empty[kslot(j)]);
         }
-        if (ok) {
+        if (ok && n1 > 0) {
           const int jl = n1 - 1;
           ok = mbar_wait(&ring_full[vslot(jl)], vpar(jl), abort_flag, status, kStatusTimeout);
           tc_fence_after();
@@ -384,6 +398,8 @@ __global__ void __launch_bounds__(384, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
     const int row = q0 + t * C::BM + r;
+    const int row_off = row + off;              // causal: key visible iff key <= row_off
+    const int tile_off = q0 + t * C::BM + off;  // ... for the tile's first row
     const int n_t = t == 0 ? n0 : n1;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = lane_base + C::COL_S + t * C::BN;
@@ -414,14 +430,14 @@ __global__ void __launch_bounds__(384, 1)
       for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(s[cc]);
 
       const int kbase = j * C::BN;
-      const bool need_mask = (kbase + C::BN > N) || (CAUSAL && kbase + C::BN - 1 > q0 + t * C::BM);
+      const bool need_mask = (kbase + C::BN > Nk) || (CAUSAL && kbase + C::BN - 1 > tile_off);
       if (need_mask) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int key = kbase + 32 * cc + i;
-            if (key >= N || (CAUSAL && key > row)) s[cc][i] = neg_inf();
+            if (key >= Nk || (CAUSAL && key > row_off)) s[cc][i] = neg_inf();
           }
       }
       float mx = s[0][0];
@@ -499,11 +515,12 @@ __global__ void __launch_bounds__(384, 1)
 
     // ------------------------------------------------------------ epilogue
     if (ok) ok = warp_wait(o_full, 0, abort_flag, status);
-    if (SPARSE && ok && c == 0) {  // no key tile kept: empty softmax, O = 0, LSE = -inf
-      uint4* orow = reinterpret_cast<uint4*>(o) + ((long long)bh * N + row) * (D / 8);
-      if (row < N) {
-        for (int q = 0; q < D / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
-        lse[(long long)bh * N + row] = neg_inf();
+    const long long frow = sv.qflat(row);
+    if (ok && c == 0) {  // no key tile for this query tile: empty softmax, O = 0, LSE = -inf
+      uint4* orow = reinterpret_cast<uint4*>(o) + frow * (dh / 8);
+      if (row < Nq) {
+        for (int q = 0; q < dh / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
+        lse[frow] = neg_inf();
       }
     } else if (ok) {
       tc_fence_after();
@@ -511,25 +528,28 @@ __global__ void __launch_bounds__(384, 1)
       // so each output row stays a convex combination of V rows; the
       // rounding of the dominant weight then cancels instead of showing up
       // at the 16-bit resolution of P.
-      const float inv_l = (DROP ? drop.keep_scale : 1.f) / l_mma;
-      // Each thread writes its own row: D/8 16-byte chunks, contiguous in memory.
-      uint4* orow = reinterpret_cast<uint4*>(o) + ((long long)bh * N + row) * (D / 8);
+      // A row that saw no key (bottom-right causal with Nq > Nk) has l = 0 and
+      // O = 0 in TMEM: it stays 0, and its LSE is -inf.
+      const float inv_l = l_mma > 0.f ? (DROP ? drop.keep_scale : 1.f) / l_mma : 0.f;
+      // Each thread writes its own row: dh/8 16-byte chunks, contiguous in memory.
+      uint4* orow = reinterpret_cast<uint4*>(o) + frow * (dh / 8);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
+        if (32 * cc >= dh) break;  // features past dh (zero-padded inputs) are not stored
         float ov[32];
         tmem_ld32(tO + 32 * cc, ov);
         tmem_ld_wait(ov);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, BF16);
-        if (row < N) {
+        if (row < Nq) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) orow[4 * cc + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
-      if (row < N) {
+      if (row < Nq) {
         const float m_fin = (m_ref == neg_inf()) ? 0.f : m_ref;
-        lse[(long long)bh * N + row] = (m_fin + __log2f(l)) * kLn2;
+        lse[frow] = (m_fin + __log2f(l)) * kLn2;
       }
     }
   }
@@ -542,16 +562,16 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL, BF16, SPARSE, DROP>;
+  auto kern = fa_fwd_kernel<D, CAUSAL, BF16, SPARSE, DROP, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int n_qblocks = (a.N + C::QT * C::BM - 1) / (C::QT * C::BM);
+  const int n_qblocks = (a.lay.Nq + C::QT * C::BM - 1) / (C::QT * C::BM);
   const long long grid = (long long)n_qblocks * a.BH;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.N, a.BH, n_qblocks,
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.lay, a.BH, n_qblocks,
                                                          a.scale_log2, a.block_mask, a.mask_heads, a.drop,
                                                          a.status);
   return cudaGetLastError();

@@ -10,6 +10,26 @@ namespace fa {
 
 // Status bits latched by kernels in the device status word.
 constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned int kStatusBadSeqlens = 2u;  // a cu_seqlens range outside the packed tensors or maxima
+
+// Where the rows of each (sequence, head) problem live.
+//   dense  (cu_q == nullptr): q/o/dq [B, H, Nq, dh], k/v/dk/dv [B, H, Nk, dh]
+//          head-major, every sequence of the same length; lse/delta [B, H, Nq].
+//   varlen (cu_q != nullptr): packed token-major q/o/dq [Tq, H, dh] and
+//          k/v/dk/dv [Tk, H, dh]; sequence b owns query rows cu_q[b] ..
+//          cu_q[b+1]-1 and key rows cu_k[b] .. cu_k[b+1]-1; lse/delta [Tq, H].
+//          Nq / Nk are then the largest sequence lengths (grid sizing only).
+// dh is the head dimension of the tensors; the kernels compute with width
+// D >= dh (dh = 96 runs the D = 128 kernels with the features 96-127 read
+// as zero by TMA and never stored).
+struct SeqLayout {
+  const int* cu_q = nullptr;
+  const int* cu_k = nullptr;
+  int H = 1;
+  int Nq = 0, Nk = 0;
+  int Tq = 0, Tk = 0;  // varlen: packed rows of q and k (bounds for the offsets)
+  int dh = 0;
+};
 
 // Dropout parameters (see fa_philox.cuh): entries whose 16-bit draw is below
 // t are dropped; kept ones are scaled by keep_scale = 65536 / (65536 - t).
@@ -21,11 +41,11 @@ struct DropParams {
 };
 
 struct FwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v;        // 3-D maps over [B*H, N, d], box {64, 128, 1}
-  void* o;                             // [B*H, N, d]
-  float* lse;                          // [B*H, N]
-  int N;
-  int BH;
+  CUtensorMap tm_q, tm_k, tm_v;        // 3-D maps, box 64 columns x 128 rows (see make_map)
+  void* o;                             // layout `lay`
+  float* lse;
+  SeqLayout lay;
+  int BH;                              // B * H
   float scale_log2;                    // scale * log2(e)
   const uint8_t* block_mask = nullptr; // [mask_heads, T, T] block mask, T = ceil(N/128); null = dense
   int mask_heads = 1;                  // 1 (shared by all heads) or B*H
@@ -35,16 +55,18 @@ struct FwdArgs {
 };
 cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_forward_dropout(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
+// Packed variable-length instances (a.lay.cu_q != nullptr), with or without dropout.
+cudaError_t launch_forward_varlen(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
-  CUtensorMap tm_q, tm_do;         // box {64, BQ, 1}
-  CUtensorMap tm_k, tm_v;          // box {64, 128, 1}
-  void* dk;                        // [B*H, N, d]
-  void* dv;                        // [B*H, N, d]
-  const float* lse;                // [B*H, N]
-  const float* delta;              // [B*H, N]
-  float* dq_accum;                 // [B*H, N, d] float32
-  int N;
+  CUtensorMap tm_q, tm_do;         // box 64 columns x BQ rows
+  CUtensorMap tm_k, tm_v;          // box 64 columns x 128 rows
+  void* dk;                        // layout `lay` (key side)
+  void* dv;
+  const float* lse;                // one float per query row
+  const float* delta;
+  float* dq_accum;                 // float32, query side, dh columns
+  SeqLayout lay;
   int BH;
   float scale;
   float scale_log2;
@@ -57,6 +79,7 @@ struct BwdArgs {
 int backward_q_tile(int d);  // query rows per inner iteration of the dK/dV kernel
 cudaError_t launch_backward_dkdv(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward_dkdv_dropout(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_backward_dkdv_varlen(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream);
 // keep[bh][i][j] = 1 if entry (bh, i, j) is kept, else 0 ([BH, Nq, Nk] bytes).
 cudaError_t launch_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, const DropParams& drop,
                                      cudaStream_t stream);

@@ -165,6 +165,22 @@ def blocksparse_inputs(w: BlockSparseWorkload):
     return q, k, v, do, block_mask(w)
 
 
+def varlen_inputs(lengths_q, lengths_k, H: int, d: int, dtype: str, seed: int, with_do: bool = True):
+    """Packed token-major q, dO [sum(lengths_q), H, d], k, v [sum(lengths_k), H, d]
+    (16-bit, N(0,1) before rounding, drawn in that order from one generator)
+    and the int32 offsets cu_q, cu_k (B + 1 entries each)."""
+    g = torch.Generator().manual_seed(seed)
+    dt = DTYPES[dtype]
+    Tq, Tk = int(sum(lengths_q)), int(sum(lengths_k))
+    q = torch.randn(Tq, H, d, generator=g).to(dt)
+    k = torch.randn(Tk, H, d, generator=g).to(dt)
+    v = torch.randn(Tk, H, d, generator=g).to(dt)
+    do = torch.randn(Tq, H, d, generator=g).to(dt) if with_do else None
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lengths_q)]), dtype=torch.int32)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lengths_k)]), dtype=torch.int32)
+    return q, k, v, do, cu_q, cu_k
+
+
 def page_inputs(N: int, D: int, seed: int):
     """float64 Q, K, V of one head, drawn like the tutorial page's demos."""
     rng = np.random.default_rng(seed)

@@ -25,8 +25,10 @@
  *   16-bit type `dtype` (FA_FP16 or FA_BF16).  LSE and D are contiguous
  *   [B, H, N] float32 arrays.  LSE is in natural-log units of the scaled
  *   scores: LSE_i = ln sum_j exp(s * q_i . k_j).
- * - Supported: d in {64, 128}; N >= 1 (any N: tails are masked); B, H >= 1
- *   with B*H*N*d < 2^31; scale finite and > 0.
+ * - Supported: d in {64, 96, 128} (split-KV decoding: 64, 128); N >= 1
+ *   (any N: tails are masked); B, H >= 1 with B*H*N*d < 2^31; scale finite
+ *   and > 0.  d = 96 runs the d = 128 kernels with features 96-127 read as
+ *   zero and never stored.
  * - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
  *   enqueue work on it and return; nothing is written to host memory and
  *   the host never waits.
@@ -37,6 +39,8 @@
  * - No exceptions cross this interface; all entry points are thread-safe
  *   (they keep no mutable host state).
  * - Outputs must not alias inputs.
+ * - Packed variable-length batches (fa_*_varlen): see the block before
+ *   fa_forward_varlen.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -55,7 +59,8 @@ typedef enum {
   FA_ERR_CUDA = 3,
   FA_ERR_TIMEOUT = 4,
   FA_ERR_WORKSPACE = 5,
-  FA_ERR_SCRATCH_TOO_SMALL = 6
+  FA_ERR_SCRATCH_TOO_SMALL = 6,
+  FA_ERR_SEQLENS = 7
 } fa_status;
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
@@ -195,6 +200,38 @@ fa_status fa_backward_dkdv_blocksparse(const void* q, const void* k, const void*
 /* Stage 3: dq = scale * dq_accum, rounded to dtype. */
 fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,
                                  float scale, void* stream);
+
+/*
+ * Packed variable-length batches.  B sequences of different lengths laid end
+ * to end in token-major tensors: q, o, dq are [total_q, H, d] and k, v, dk, dv
+ * are [total_k, H, d] (16-bit, contiguous); lse is [total_q, H] float32 (the
+ * same flat order as the rows of q).  cu_seqlens_q and cu_seqlens_k are
+ * device int32 arrays of B + 1 offsets: sequence b owns query rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1]-1 (cu[0] = 0, non-decreasing, cu[B] = total).  Each
+ * sequence is an independent attention problem ("FlashAttention 为什么不需要存下
+ * 注意力矩阵", section 3, applied per sequence); under the causal mask the
+ * diagonal is aligned bottom-right: query i of a sequence with Nq queries and
+ * Nk keys sees key j iff j <= i + Nk - Nq, and a query that sees no key (and
+ * every query of a sequence with no key) gets O = 0 and LSE = -inf, and dQ = 0.
+ * max_seqlen_q / max_seqlen_k (host ints) bound the per-sequence lengths and
+ * size the grid.  The offsets are read on the device only: a sequence whose
+ * range leaves [0, total] or exceeds the maxima is skipped and FA_ERR_SEQLENS
+ * is latched for fa_device_status().  p_drop, seed, offset: dropout as for
+ * fa_forward_dropout (p_drop = 0: none), with the query index counted within
+ * its sequence and bh = b * H + h.  The backward workspace holds
+ * fa_backward_varlen_workspace_size(total_q, H, d) bytes (256-byte aligned).
+ */
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                            const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k, int total_q,
+                            int total_k, int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                            uint32_t offset, void* stream);
+size_t fa_backward_varlen_workspace_size(int total_q, int H, int d);
+fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                             const float* lse, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                             const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k, int total_q,
+                             int total_k, int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
+                             uint32_t offset, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Split-KV forward for few queries against many keys (decoding).

@@ -49,7 +49,7 @@ def test_status_strings(lib):
 
 def test_workspace_size_is_linear_in_n(lib):
     ws = lib.fa_backward_workspace_size
-    assert ws(1, 1, 0, 64) == 0 and ws(1, 1, 16, 96) == 0
+    assert ws(1, 1, 0, 64) == 0 and ws(1, 1, 16, 80) == 0 and ws(1, 1, 16, 96) == 16 * (4 + 4 * 96) + 192
     a, b = ws(2, 32, 8192, 128), ws(2, 32, 16384, 128)
     assert a == 2 * 32 * 8192 * (4 + 4 * 128)
     assert b == 2 * a
@@ -63,7 +63,7 @@ def test_forward_rejects_bad_arguments(lib, case):
     if case == "null":
         args["q"] = None
     elif case == "bad_d":
-        args["d"], want = 96, 2
+        args["d"], want = 80, 2
     elif case == "bad_dtype":
         args["dt"], want = 7, 2
     elif case == "bad_scale":
@@ -111,7 +111,7 @@ def test_blocksparse_mask_validation(lib):
                                               1, 0, 0.125, None)
         assert rc == 1
     # shape errors still come first with a valid mask count
-    rc = lib.fa_forward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, 6, 2, 3, 300, 96, 1, 0, 0.125, None)
+    rc = lib.fa_forward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, 6, 2, 3, 300, 80, 1, 0, 0.125, None)
     assert rc == 2
 
 
@@ -130,3 +130,28 @@ def test_dropout_validation(lib):
         assert lib.fa_dropout_keep_mask(ptr, 1, 4, 4, p, 1, 0, None) == 1
     assert lib.fa_dropout_keep_mask(None, 1, 4, 4, 0.5, 1, 0, None) == 1
     assert lib.fa_dropout_keep_mask(ptr, 0, 4, 4, 0.5, 1, 0, None) == 1
+
+
+def test_varlen_validation(lib):
+    """Host-side checks of the packed variable-length entry points (the
+    offsets themselves are only read on the device)."""
+    ptr = 1 << 20
+    good = dict(B=2, H=3, mq=100, mk=120, tq=150, tk=200, d=64)
+
+    def fwd(cu_q=ptr, cu_k=ptr, **kw):
+        a = dict(good, **kw)
+        return lib.fa_forward_varlen(ptr, ptr, ptr, ptr, ptr, cu_q, cu_k, a["B"], a["H"], a["mq"], a["mk"], a["tq"],
+                                     a["tk"], a["d"], 1, 1, 0.125, 0.0, 0, 0, None)
+
+    assert fwd(cu_q=None) == 1 and fwd(cu_k=ptr + 2) == 1
+    assert fwd(B=0) == 1 and fwd(mq=0) == 1 and fwd(tk=0) == 1
+    assert fwd(d=80) == 2
+    rc = lib.fa_forward_varlen(ptr, ptr, ptr, ptr, ptr, ptr, ptr, 2, 3, 100, 120, 150, 200, 64, 1, 1, 0.125, 1.5, 0,
+                               0, None)
+    assert rc == 1  # bad dropout probability
+    ws = lib.fa_backward_varlen_workspace_size
+    assert ws(150, 3, 96) == ((150 * 3 * 4 + 255) // 256) * 256 + 150 * 3 * 96 * 4
+    assert ws(0, 3, 64) == 0 and ws(10, 3, 80) == 0
+    rc = lib.fa_backward_varlen(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 2, 3, 100, 120, 150, 200, 64,
+                                1, 1, 0.125, 0.0, 0, 0, ptr, 16, None)
+    assert rc == 5  # workspace too small
