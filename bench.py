@@ -267,6 +267,32 @@ def block_mask_flops(w, bm) -> float:
     return 4.0 * w.d * float(total)
 
 
+def varlen_pairs(lengths, causal) -> float:
+    """(query, key) pairs computed over a packed batch with Nq = Nk per sequence."""
+    return float(sum(n * (n + 1) // 2 if causal else n * n for n in lengths))
+
+
+def oracle_varlen_sample(w, budget_s: float):
+    """float64 oracle on whole (sequence, head) problems of a packed batch, in
+    order, until `budget_s` is spent; TFLOP/s in the 2.5 F convention."""
+    from exact_io_aware_forward_gb300.synth import as_float64, attention_inputs
+    from oracle import attention as A
+    scale = 1.0 / math.sqrt(w.d)
+    done, spent, flops = 0, 0.0, 0.0
+    for n in sorted(w.lengths):  # shortest first so that the sample covers several sequences
+        if done and spent >= budget_s:
+            break
+        q, k, v, do = as_float64(*attention_inputs(1, 1, n, w.d, w.dtype, seed=w.seed * 1000 + done))
+        t0 = time.perf_counter()
+        A.forward_head(q[0, 0], k[0, 0], v[0, 0], scale, w.causal)
+        A.backward_head(q[0, 0], k[0, 0], v[0, 0], do[0, 0], scale, w.causal)
+        spent += time.perf_counter() - t0
+        flops += 2.5 * 4.0 * w.d * varlen_pairs([n], w.causal)
+        done += 1
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return flops / spent / 1e12, done, spent, threads
+
+
 def oracle_variant_sample(kind, w, bm, budget_s: float, max_heads: int):
     """float64 oracle (forward + explicit backward) on whole heads of a
     block-sparse or dropout workload until `budget_s` is spent; TFLOP/s in the
@@ -308,36 +334,56 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
     import torch
 
     import exact_io_aware_forward_gb300 as fa
-    from exact_io_aware_forward_gb300.synth import blocksparse_inputs, workload_inputs
+    from exact_io_aware_forward_gb300.synth import blocksparse_inputs, varlen_workload_inputs, workload_inputs
 
+    cu_q = cu_k = None
     if kind == "blocksparse":
         q, k, v, do, bm = blocksparse_inputs(w)
         md = torch.from_numpy(bm.astype("uint8")).to(dev)
+    elif kind == "varlen":
+        q, k, v, do, cu_q, cu_k = varlen_workload_inputs(w)
+        cu_q, cu_k = cu_q.to(dev), cu_k.to(dev)
+        bm = md = None
     else:
         q, k, v, do = workload_inputs(w)
         bm = md = None
     q, k, v, do = (x.to(dev) for x in (q, k, v, do))
-    B, H, N, d = w.B, w.H, w.N, w.d
+    d = w.d
+    if kind == "varlen":  # packed [T, H, d]; the flat [1, 1, T*H, d] view serves the row-wise stages
+        T, H = q.shape[0], q.shape[1]
+        rows = T * H
+        lse = torch.empty((T, H), device=dev, dtype=torch.float32)
+        ws = torch.empty(fa.fa_backward_varlen_workspace_size(T, H, d), device=dev, dtype=torch.uint8)
+        shape_r = (T, H)
+        maxlen = max(w.lengths)
+    else:
+        B, H, N = w.B, w.H, w.N
+        rows = B * H * N
+        lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        ws = torch.empty(fa.fa_backward_workspace_size(B, H, N, d), device=dev, dtype=torch.uint8)
+        shape_r = (B, H, N)
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    ws = torch.empty(fa.fa_backward_workspace_size(B, H, N, d), device=dev, dtype=torch.uint8)
-    rows = B * H * N
-    delta = ws[: rows * 4].view(torch.float32).view(B, H, N)
+    delta = ws[: rows * 4].view(torch.float32).view(*shape_r)
     off = (rows * 4 + 255) // 256 * 256
-    acc = ws[off: off + rows * d * 4].view(torch.float32).view(B, H, N, d)
+    acc = ws[off: off + rows * d * 4].view(torch.float32).view(*q.shape)
+    flat = (lambda x: x.view(1, 1, rows, -1)) if kind == "varlen" else (lambda x: x)
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
 
     def fwd():
         if kind == "blocksparse":
             fa.fa_forward_blocksparse(q, k, v, o, lse, md, w.causal)
+        elif kind == "varlen":
+            fa.fa_forward_varlen(q, k, v, o, lse, cu_q, cu_k, maxlen, maxlen, w.causal)
         else:
             fa.fa_forward_dropout(q, k, v, o, lse, DROP_P, DROP_SEED, DROP_OFFSET, w.causal)
 
     def dkdv():
         if kind == "blocksparse":
             fa.fa_backward_dkdv_blocksparse(q, k, v, do, lse, delta, acc, dk, dv, md, w.causal)
+        elif kind == "varlen":
+            fa.fa_backward_dkdv_varlen(q, k, v, do, lse, delta, acc, dk, dv, cu_q, cu_k, maxlen, maxlen, w.causal)
         else:
             fa.fa_backward_dkdv_dropout(q, k, v, do, lse, delta, acc, dk, dv, DROP_P, DROP_SEED, DROP_OFFSET,
                                         w.causal)
@@ -346,11 +392,12 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
         if e: e[0].record(stream)
         fwd()
         if e: e[1].record(stream)
-        fa.fa_backward_preprocess(o, do, delta, acc)
+        fa.fa_backward_preprocess(flat(o), flat(do), delta.view(1, 1, rows) if kind == "varlen" else delta,
+                                  flat(acc))
         if e: e[2].record(stream)
         dkdv()
         if e: e[3].record(stream)
-        fa.fa_backward_dq_convert(acc, dq)
+        fa.fa_backward_dq_convert(flat(acc), flat(dq), scale=1.0 / math.sqrt(d))
         if e: e[4].record(stream)
 
     for _ in range(warmup):
@@ -369,21 +416,27 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
     clocks = sampler.stop() if sampler else None
     fa.fa_device_status()
     parts = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps for j in range(4)]
-    return t0.elapsed_time(t1) / steps, parts, clocks, (q, k, v, do, md, ws, bm)
+    extra = (cu_q, cu_k) if kind == "varlen" else md
+    return t0.elapsed_time(t1) / steps, parts, clocks, (q, k, v, do, extra, ws, bm)
 
 
 def variant_flops(kind, w, bm):
-    return block_mask_flops(w, bm) if kind == "blocksparse" else w.fwd_flops()
+    if kind == "blocksparse":
+        return block_mask_flops(w, bm)
+    if kind == "varlen":
+        return 4.0 * w.d * w.H * varlen_pairs(w.lengths, w.causal)
+    return w.fwd_flops()
 
 
 def run_variant(args, world, rank, local, kind):
-    """The JSON line of `--mode blocksparse` (S1) or `--mode dropout` (C4 with p = 0.1)."""
+    """The JSON line of `--mode blocksparse` (S1), `--mode dropout` (C4 with p = 0.1)
+    or `--mode varlen` (V1)."""
     import torch
 
     import exact_io_aware_forward_gb300 as fa
-    from exact_io_aware_forward_gb300.synth import C4, S1
+    from exact_io_aware_forward_gb300.synth import C4, S1, V1
 
-    w = S1 if kind == "blocksparse" else C4
+    w = {"blocksparse": S1, "varlen": V1}.get(kind, C4)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
@@ -392,18 +445,29 @@ def run_variant(args, world, rank, local, kind):
     F = variant_flops(kind, w, bm)
     value = 2.5 * F / (ms * 1e-3) / 1e12
     hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
-    hm = md.cpu().pin_memory() if md is not None else None
+    hm = None
+    if kind == "blocksparse":
+        hm = md.cpu().pin_memory()
+    elif kind == "varlen":
+        hm = tuple(x.cpu().pin_memory() for x in md)  # cu_seqlens_q, cu_seqlens_k
     ho, hdq, hdk, hdv = (torch.empty_like(x, device="cpu").pin_memory() for x in (q, q, q, q))
-    hlse = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    hlse = torch.empty(q.shape[:2] if kind == "varlen" else (w.B, w.H, w.N), dtype=torch.float32).pin_memory()
     extra = {"block_mask": None} if kind == "blocksparse" else \
         {"dropout_p": DROP_P, "seed": DROP_SEED, "offset": DROP_OFFSET}
 
     def e2e_step():
         gq, gk, gv, gdo = (x.to(dev, non_blocking=True) for x in (hq, hk, hv, hdo))
-        if kind == "blocksparse":
-            extra["block_mask"] = hm.to(dev, non_blocking=True)
-        go, glse = fa.forward(gq, gk, gv, causal=w.causal, **extra)
-        gdq, gdk, gdv = fa.backward(gq, gk, gv, go, glse, gdo, causal=w.causal, workspace=ws, **extra)
+        if kind == "varlen":
+            cq, ck = (x.to(dev, non_blocking=True) for x in hm)
+            L = max(w.lengths)
+            go, glse = fa.forward_varlen(gq, gk, gv, cq, ck, L, L, causal=w.causal)
+            gdq, gdk, gdv = fa.backward_varlen(gq, gk, gv, go, glse, gdo, cq, ck, L, L, causal=w.causal,
+                                               workspace=ws)
+        else:
+            if kind == "blocksparse":
+                extra["block_mask"] = hm.to(dev, non_blocking=True)
+            go, glse = fa.forward(gq, gk, gv, causal=w.causal, **extra)
+            gdq, gdk, gdv = fa.backward(gq, gk, gv, go, glse, gdo, causal=w.causal, workspace=ws, **extra)
         for h, g in ((ho, go), (hlse, glse), (hdq, gdq), (hdk, gdk), (hdv, gdv)):
             h.copy_(g, non_blocking=True)
 
@@ -421,8 +485,20 @@ def run_variant(args, world, rank, local, kind):
     peak = float(peaks["bf16_tflops"])
     dkdv = 2.5 * F / (parts[2] * 1e-3) / 1e12
     fwd = F / (parts[0] * 1e-3) / 1e12
-    cpu, heads, spent, threads = oracle_variant_sample(kind, w, bm, args.cpu_budget, 64)
-    if kind == "blocksparse":
+    if kind == "varlen":
+        cpu, heads, spent, threads = oracle_varlen_sample(w, args.cpu_budget)
+    else:
+        cpu, heads, spent, threads = oracle_variant_sample(kind, w, bm, args.cpu_budget, 64)
+    if kind == "varlen":
+        metric = "variable-length attention TFLOPS over the packed batch (fwd+bwd = 2.5 F)"
+        data = "synthetic (seeded N(0,1) packed Q, K, V, dO; seeded uniform sequence lengths; no dataset)"
+        cfg = {"B": w.B, "lengths": list(w.lengths), "total_tokens": int(sum(w.lengths)),
+               "flop_count": "F = 4*d*H per (query, key) pair of every sequence (causal: N(N+1)/2 pairs)"}
+        kern = "fa_bwd_dkdv_kernel<128,causal,bf16,varlen>"
+        alg = "10*d*H per (query, key) pair of every sequence (5 GEMMs), per launch"
+        h2d_extra = 2 * 4 * (w.B + 1)
+        what = "(the shortest sequences first)"
+    elif kind == "blocksparse":
         metric = "block-sparse attention TFLOPS over kept blocks (fwd+bwd = 2.5 F)"
         data = "synthetic (seeded N(0,1) Q, K, V, dO; seeded random block mask; no dataset)"
         cfg = {"density": w.density, "kept_blocks": int(bm.sum()), "mask_heads": int(bm.shape[0]),
@@ -444,7 +520,8 @@ def run_variant(args, world, rank, local, kind):
         "metric": metric, "value": round(world * value, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": data,
-        "config": dict({"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+        "config": dict({"workload": w.name, "B": w.B, "H": w.H, "N": getattr(w, "N", None), "d": w.d,
+                        "causal": w.causal,
                         "l2": "inputs larger than L2 (each of Q, K, V, dO is %.0f MB > 129 MB)" % (elem / 1e6)},
                        **cfg),
         "fwd_tflops": round(fwd, 1), "fwd_frac_of_peak": round(fwd / peak, 4),
@@ -456,7 +533,7 @@ def run_variant(args, world, rank, local, kind):
                      "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic": alg},
         "e2e": {"value": round(world * 2.5 * F / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(4 * elem + h2d_extra),
-                "d2h_bytes_per_step": int(4 * elem + w.B * w.H * w.N * 4), "ms_per_step": round(e2e_ms, 3)},
+                "d2h_bytes_per_step": int(4 * elem + hlse.numel() * 4), "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "cpu_baseline": {"value": cpu, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -612,7 +689,8 @@ def run_gpu(args, w, world, rank, local):
         result["decode"] = {"workload": D1.name, "ms": round(dms, 4), "GB_per_s": round(dgbs, 1),
                             "frac_of_hbm_peak": round(dgbs / float(peaks["hbm_gbs"]), 4)}
         from exact_io_aware_forward_gb300.synth import S1
-        for kind, vw in (("blocksparse", S1), ("dropout", w)):
+        from exact_io_aware_forward_gb300.synth import V1
+        for kind, vw in (("blocksparse", S1), ("dropout", w), ("varlen", V1)):
             sms, sparts, _, sbufs = measure_variant(dev, kind, vw, 10, 3)
             sF = variant_flops(kind, vw, sbufs[-1])
             result[kind] = {"workload": vw.name + (f" p={DROP_P}" if kind == "dropout" else ""),
@@ -657,10 +735,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="C4", help="C2, C3N, C3C, C4 or C5")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--mode", default="train", choices=["train", "decode", "blocksparse", "dropout"],
+    ap.add_argument("--mode", default="train", choices=["train", "decode", "blocksparse", "dropout", "varlen"],
                     help="train: fwd+bwd step (the headline); decode: split-KV decoding line; "
                          "blocksparse: fwd+bwd under a 128x128 block mask; dropout: fwd+bwd of the "
-                         "training workload with dropout p=0.1")
+                         "training workload with dropout p=0.1; varlen: fwd+bwd of a packed batch of "
+                         "16 causal sequences")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing (rank 0, N=1)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
@@ -668,7 +747,7 @@ def main():
     from exact_io_aware_forward_gb300.synth import WORKLOADS
     w = WORKLOADS[args.workload]
     world, rank, local = dist_env()
-    if args.impl == "ours" and args.mode in ("decode", "blocksparse", "dropout"):
+    if args.impl == "ours" and args.mode in ("decode", "blocksparse", "dropout", "varlen"):
         from exact_io_aware_forward_gb300 import build as fa_build
         fa_build.build()
         if args.mode == "decode":

@@ -46,6 +46,8 @@ SIGNATURES = {
     "fa_backward_varlen_workspace_size": (_S, [_I, _I, _I]),
     "fa_backward_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                                 _F, _U64, _U32, _P, _S, _P]),
+    "fa_backward_dkdv_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                     _I, _F, _F, _U64, _U32, _P]),
     "fa_device_status": (_I, [_P]),
 }
 

@@ -399,6 +399,20 @@ fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const 
                       stream, &dp);
 }
 
+fa_status fa_backward_dkdv_varlen(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                  const float* delta, float* dq_accum, void* dk, void* dv, const int* cu_seqlens_q,
+                                  const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k,
+                                  int total_q, int total_k, int d, int dtype, int causal, float scale, float p_drop,
+                                  uint64_t seed, uint32_t offset, void* stream) {
+  Shape s;
+  const fa_status st = varlen_shape(cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, max_seqlen_k, total_q, total_k,
+                                    d, dtype, &s);
+  if (st != FA_OK) return st;
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, causal, scale, stream, &dp);
+}
+
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* delta, float* dq_accum, int B, int H,
                                  int N, int d, int dtype, void* stream) {
   Shape s;

@@ -165,6 +165,37 @@ def blocksparse_inputs(w: BlockSparseWorkload):
     return q, k, v, do, block_mask(w)
 
 
+@dataclasses.dataclass(frozen=True)
+class VarlenWorkload:
+    """A packed batch of sequences of different lengths (query = key lengths)."""
+
+    name: str
+    H: int
+    d: int
+    dtype: str
+    causal: bool
+    lengths: tuple
+    seed: int
+
+    @property
+    def B(self) -> int:
+        return len(self.lengths)
+
+
+def _lengths(n: int, lo: int, hi: int, seed: int) -> tuple:
+    return tuple(int(x) for x in np.random.default_rng(seed).integers(lo, hi + 1, size=n))
+
+
+# Variable-length workload: 16 causal sequences of 256 .. 8192 tokens (uniform), the
+# head shape of the long training problem.
+V1 = VarlenWorkload("V1 varlen 16 seqs of 256-8192 tokens H=32 d=128 bf16 causal", 32, 128, "bf16", True,
+                    _lengths(16, 256, 8192, 8), 8)
+
+
+def varlen_workload_inputs(w: VarlenWorkload):
+    return varlen_inputs(w.lengths, w.lengths, w.H, w.d, w.dtype, w.seed)
+
+
 def varlen_inputs(lengths_q, lengths_k, H: int, d: int, dtype: str, seed: int, with_do: bool = True):
     """Packed token-major q, dO [sum(lengths_q), H, d], k, v [sum(lengths_k), H, d]
     (16-bit, N(0,1) before rounding, drawn in that order from one generator)

@@ -232,6 +232,18 @@ fa_status fa_backward_varlen(const void* q, const void* k, const void* v, const 
                              const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k, int total_q,
                              int total_k, int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
                              uint32_t offset, void* workspace, size_t workspace_bytes, void* stream);
+/*
+ * Stage 2 of fa_backward_varlen (the dK/dV kernel alone).  Stages 1 and 3 are
+ * fa_backward_preprocess and fa_backward_dq_convert called with B = 1, H = 1,
+ * N = total_q * H: they treat the packed rows as one flat [rows, d] array.
+ * delta [total_q, H] and dq_accum [total_q, H, d] float32 as in the workspace
+ * of fa_backward_varlen (delta first, dq_accum at the next 256-byte boundary).
+ */
+fa_status fa_backward_dkdv_varlen(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                  const float* delta, float* dq_accum, void* dk, void* dv, const int* cu_seqlens_q,
+                                  const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k,
+                                  int total_q, int total_k, int d, int dtype, int causal, float scale, float p_drop,
+                                  uint64_t seed, uint32_t offset, void* stream);
 
 /*
  * Split-KV forward for few queries against many keys (decoding).

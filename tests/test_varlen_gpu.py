@@ -154,3 +154,28 @@ def test_head_dim_96_dense(causal, N, dtype):
         assert float(np.abs(lse[0, h].double().cpu().numpy() - rl).max()) <= LSE_TOL
         for g, r in zip((dq, dk, dv), A.backward_head(qf[0, h], kf[0, h], vf[0, h], dof[0, h], s, causal)):
             assert rel_fro(g[0, h].double().cpu().numpy(), r) <= GRAD_REL_FRO
+
+
+def test_varlen_stages_equal_the_full_call():
+    """preprocess / convert on the flat [total_q * H, d] rows plus the varlen
+    dK/dV stage (the launches the benchmark times one by one) give what
+    fa_backward_varlen gives."""
+    lq = [300, 129, 700]
+    q, k, v, do, cu_q, cu_k = (x.to(DEV) for x in varlen_inputs(lq, lq, 2, 128, "bf16", seed=31))
+    L = max(lq)
+    o, lse = fa.forward_varlen(q, k, v, cu_q, cu_k, L, L, causal=True)
+    dq, dk, dv = fa.backward_varlen(q, k, v, o, lse, do, cu_q, cu_k, L, L, causal=True)
+    T, H, d = q.shape
+    rows = T * H
+    ws = torch.empty(fa.fa_backward_varlen_workspace_size(T, H, d), device=DEV, dtype=torch.uint8)
+    delta = ws[: rows * 4].view(torch.float32)
+    off = (rows * 4 + 255) // 256 * 256
+    acc = ws[off: off + rows * d * 4].view(torch.float32).view(T, H, d)
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flat = lambda x: x.view(1, 1, rows, -1)  # noqa: E731
+    fa.fa_backward_preprocess(flat(o), flat(do), delta.view(1, 1, rows), flat(acc))
+    fa.fa_backward_dkdv_varlen(q, k, v, do, lse, delta.view(T, H), acc, dk2, dv2, cu_q, cu_k, L, L, causal=True)
+    fa.fa_backward_dq_convert(flat(acc), flat(dq2), scale=1 / math.sqrt(d))
+    fa.fa_device_status()
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert float((dq.float() - dq2.float()).abs().max()) <= 1e-2 * float(dq.float().abs().max())
