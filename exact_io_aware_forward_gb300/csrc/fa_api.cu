@@ -50,12 +50,12 @@ struct Shape {
   bool varlen() const { return lay.cu_q != nullptr; }
   long long q_rows() const { return varlen() ? (long long)lay.Tq * H : (long long)B * H * lay.Nq; }
   bool bf16() const { return dtype == FA_BF16; }
-  int width() const { return d == 64 ? 64 : 128; }  // compute width of the kernels (96 runs at 128)
+  int width() const { return d == 64 ? 64 : d == 256 ? 256 : 128; }  // compute width (96 runs at 128)
 };
 
 fa_status check_dims(int d, int dtype) {
   if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -172,9 +172,11 @@ fa_status run_forward(const Shape& s, const void* q, const void* k, const void* 
   if (st != FA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
+  if (s.d == 256 && block_mask) return FA_ERR_UNSUPPORTED;
+  const int kv_rows = s.d == 256 ? 64 : 128;  // the d = 256 kernel streams 64-key tiles
   fa::FwdArgs a;
-  if (!make_map(&a.tm_q, q, s, false, 128) || !make_map(&a.tm_k, k, s, true, 128) ||
-      !make_map(&a.tm_v, v, s, true, 128))
+  if (!make_map(&a.tm_q, q, s, false, 128) || !make_map(&a.tm_k, k, s, true, kv_rows) ||
+      !make_map(&a.tm_v, v, s, true, kv_rows))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;
@@ -189,7 +191,8 @@ fa_status run_forward(const Shape& s, const void* q, const void* k, const void* 
   a.dropout = drop != nullptr && drop->t > 0;
   if (a.dropout) a.drop = *drop;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = s.varlen()  ? fa::launch_forward_varlen(s.width(), causal != 0, s.bf16(), a, cs)
+  const cudaError_t e = s.d == 256   ? fa::launch_forward256(causal != 0, s.bf16(), a, cs)
+                        : s.varlen()  ? fa::launch_forward_varlen(s.width(), causal != 0, s.bf16(), a, cs)
                         : a.dropout ? fa::launch_forward_dropout(s.width(), causal != 0, s.bf16(), a, cs)
                                     : fa::launch_forward(s.width(), causal != 0, s.bf16(), a, cs);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -197,6 +200,7 @@ fa_status run_forward(const Shape& s, const void* q, const void* k, const void* 
 
 fa_status run_preprocess(const Shape& s, const void* o, const void* dO, float* delta, float* dq_accum,
                          void* stream) {
+  if (s.d == 256) return FA_ERR_UNSUPPORTED;  // the backward pass has no d = 256 kernels
   if (!aligned16(o) || !aligned16(dO) || !aligned16(delta) || !aligned16(dq_accum)) return FA_ERR_INVALID_ARG;
   if (fa::launch_backward_preprocess(s.d, s.bf16(), o, dO, delta, dq_accum, s.q_rows(),
                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -209,6 +213,7 @@ fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, 
                    int mask_heads, int causal, float scale, void* stream, const fa::DropParams* drop) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
+  if (s.d == 256) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(delta) || !aligned16(dq_accum) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
@@ -242,6 +247,7 @@ fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, 
 fa_status run_convert(const Shape& s, const float* dq_accum, void* dq, float scale, void* stream) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
+  if (s.d == 256) return FA_ERR_UNSUPPORTED;
   if (!aligned16(dq_accum) || !aligned16(dq)) return FA_ERR_INVALID_ARG;
   if (fa::launch_backward_dq_convert(s.d, s.bf16(), dq_accum, dq, s.q_rows(), scale,
                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -260,6 +266,7 @@ fa_status run_backward(const Shape& s, const void* q, const void* k, const void*
                        const fa::DropParams* drop) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
+  if (s.d == 256) return FA_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < workspace_bytes_for(s))
     return FA_ERR_WORKSPACE;
   float* delta = static_cast<float*>(workspace);
@@ -282,7 +289,8 @@ const char* fa_status_string(int status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null/misaligned pointer, bad size or bad scale";
     case FA_ERR_UNSUPPORTED:
-      return "FA_ERR_UNSUPPORTED: head dim must be 64, 96 or 128, dtype fp16/bf16, rows*H*d < 2^31";
+      return "FA_ERR_UNSUPPORTED: head dim must be 64, 96, 128 (or 256, forward only), dtype fp16/bf16, "
+             "rows*H*d < 2^31";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA launch or the stream failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up waiting on its pipeline";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing, misaligned or too small";

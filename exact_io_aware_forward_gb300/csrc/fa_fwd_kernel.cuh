@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(384, 1)
     // 0, 1, ... when DROP): drawn while the tensor core works, so that the
     // generator stays off the path from S to P.
     uint32_t keep[4] = {0u, 0u, 0u, 0u};
-    if (DROP && n_t > 0) tile_keep_bits(keep, 0, row, bh, drop.offset, drop.k0, drop.k1, drop.t);
+    if (DROP && n_t > 0) tile_keep_bits<4>(keep, 0, row, bh, drop.offset, drop.k0, drop.k1, drop.t);
     for (int j = 0; j < n_t; ++j) {
       if constexpr (SPARSE) {
         if (!(t == 0 ? act0(j) : act1(j))) continue;
@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
-      if (DROP && j + 1 < n_t) tile_keep_bits(keep, (j + 1) * C::BN, row, bh, drop.offset, drop.k0, drop.k1, drop.t);
+      if (DROP && j + 1 < n_t) tile_keep_bits<4>(keep, (j + 1) * C::BN, row, bh, drop.offset, drop.k0, drop.k1, drop.t);
       float a, b;
       f2_unpack(sum2, a, b);
       l += a + b;

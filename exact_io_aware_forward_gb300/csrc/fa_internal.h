@@ -57,6 +57,9 @@ cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cuda
 cudaError_t launch_forward_dropout(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 // Packed variable-length instances (a.lay.cu_q != nullptr), with or without dropout.
 cudaError_t launch_forward_varlen(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
+// Head dimension 256 (dense or packed, with or without dropout; no block mask):
+// K / V tensor maps with 64-row boxes.
+cudaError_t launch_forward256(bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_do;         // box 64 columns x BQ rows

@@ -49,14 +49,16 @@ __device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t t) {
   return b;
 }
 
-// Keep bits of the 128 keys [kbase, kbase + 128) of query `row`, one word per
-// 32 keys: in word cc, bit i is the even key kbase + 32cc + 2i of pair i and
-// bit 16 + i the odd key kbase + 32cc + 2i + 1 (16 generator calls).
-__device__ __forceinline__ void tile_keep_bits(uint32_t (&eo)[4], int kbase, int row, int bh, uint32_t offset,
+// Keep bits of the 32 * NW keys [kbase, kbase + 32 NW) of query `row`, one
+// word per 32 keys: in word cc, bit i is the even key kbase + 32cc + 2i of
+// pair i and bit 16 + i the odd key kbase + 32cc + 2i + 1 (4 NW generator
+// calls).
+template <int NW>
+__device__ __forceinline__ void tile_keep_bits(uint32_t (&eo)[NW], int kbase, int row, int bh, uint32_t offset,
                                                uint32_t k0, uint32_t k1, uint32_t t) {
   const uint32_t tt = t | (t << 16);
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
+  for (int cc = 0; cc < NW; ++cc) {
     uint32_t e = 0;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {

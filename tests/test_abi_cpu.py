@@ -155,3 +155,12 @@ def test_varlen_validation(lib):
     rc = lib.fa_backward_varlen(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 2, 3, 100, 120, 150, 200, 64,
                                 1, 1, 0.125, 0.0, 0, 0, ptr, 16, None)
     assert rc == 5  # workspace too small
+
+
+def test_head_dim_256_is_forward_only(lib):
+    ptr = 1 << 20
+    assert lib.fa_backward_workspace_size(1, 1, 64, 256) > 0  # shape accepted ...
+    rc = lib.fa_backward(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 64, 256, 1, 0, 0.0625, ptr, 1 << 30, None)
+    assert rc == 2  # ... but the backward pass refuses it
+    rc = lib.fa_forward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 1, 64, 256, 1, 0, 0.0625, None)
+    assert rc == 2
