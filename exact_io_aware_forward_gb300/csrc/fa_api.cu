@@ -200,7 +200,6 @@ fa_status run_forward(const Shape& s, const void* q, const void* k, const void* 
 
 fa_status run_preprocess(const Shape& s, const void* o, const void* dO, float* delta, float* dq_accum,
                          void* stream) {
-  if (s.d == 256) return FA_ERR_UNSUPPORTED;  // the backward pass has no d = 256 kernels
   if (!aligned16(o) || !aligned16(dO) || !aligned16(delta) || !aligned16(dq_accum)) return FA_ERR_INVALID_ARG;
   if (fa::launch_backward_preprocess(s.d, s.bf16(), o, dO, delta, dq_accum, s.q_rows(),
                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -213,7 +212,7 @@ fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, 
                    int mask_heads, int causal, float scale, void* stream, const fa::DropParams* drop) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  if (s.d == 256) return FA_ERR_UNSUPPORTED;
+  if (s.d == 256 && block_mask) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(delta) || !aligned16(dq_accum) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
@@ -247,7 +246,6 @@ fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, 
 fa_status run_convert(const Shape& s, const float* dq_accum, void* dq, float scale, void* stream) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  if (s.d == 256) return FA_ERR_UNSUPPORTED;
   if (!aligned16(dq_accum) || !aligned16(dq)) return FA_ERR_INVALID_ARG;
   if (fa::launch_backward_dq_convert(s.d, s.bf16(), dq_accum, dq, s.q_rows(), scale,
                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -266,7 +264,7 @@ fa_status run_backward(const Shape& s, const void* q, const void* k, const void*
                        const fa::DropParams* drop) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  if (s.d == 256) return FA_ERR_UNSUPPORTED;
+  if (s.d == 256 && block_mask) return FA_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < workspace_bytes_for(s))
     return FA_ERR_WORKSPACE;
   float* delta = static_cast<float*>(workspace);
@@ -289,7 +287,7 @@ const char* fa_status_string(int status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null/misaligned pointer, bad size or bad scale";
     case FA_ERR_UNSUPPORTED:
-      return "FA_ERR_UNSUPPORTED: head dim must be 64, 96, 128 (or 256, forward only), dtype fp16/bf16, "
+      return "FA_ERR_UNSUPPORTED: head dim must be 64, 96, 128 or 256 (no block mask at 256), dtype fp16/bf16, "
              "rows*H*d < 2^31";
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA launch or the stream failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up waiting on its pipeline";

@@ -4,7 +4,7 @@
 
 namespace fa {
 
-int backward_q_tile(int d) { return d == 128 ? 64 : 128; }
+int backward_q_tile(int d) { return d == 64 ? 128 : 64; }
 
 namespace {
 
@@ -28,6 +28,13 @@ cudaError_t launch_backward_dkdv(int d, bool causal, bool bf16, const BwdArgs& a
   FA_BWD_CASE(128, true, false)
   FA_BWD_CASE(128, true, true)
 #undef FA_BWD_CASE
+  // d = 256: dense only (no block-mask instance)
+  if (d == 256 && !a.block_mask) {
+    if (causal && bf16) return launch_dkdv_t<256, true, true, false, false, false>(a, stream);
+    if (causal) return launch_dkdv_t<256, true, false, false, false, false>(a, stream);
+    if (bf16) return launch_dkdv_t<256, false, true, false, false, false>(a, stream);
+    return launch_dkdv_t<256, false, false, false, false, false>(a, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -47,13 +47,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // One row is handled by TPR consecutive threads (a power of two), VPT
-// 16-byte vectors (8 elements) each: D = 64: 8 x 1, 96: 4 x 3, 128: 16 x 1.
+// 16-byte vectors (8 elements) each: D = 64: 8 x 1, 96: 4 x 3, 128: 16 x 1,
+// 256: 16 x 2.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __restrict__ o,
                                                                 const uint4* __restrict__ dO,
                                                                 float* __restrict__ delta,
                                                                 float4* __restrict__ dq_accum, long long rows) {
-  constexpr int TPR = D == 96 ? 4 : D / 8;
+  constexpr int TPR = D == 96 ? 4 : D == 256 ? 16 : D / 8;
   constexpr int VPT = D / 8 / TPR;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const int part = threadIdx.x % TPR;
@@ -117,7 +118,7 @@ int grid_for(long long threads_needed) {
 
 cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const void* dO, float* delta,
                                        float* dq_accum, long long rows, cudaStream_t stream) {
-  const long long threads = rows * (d == 96 ? 4 : d / 8);
+  const long long threads = rows * (d == 96 ? 4 : d == 256 ? 16 : d / 8);
   const int grid = grid_for(threads);
   const uint4* o4 = static_cast<const uint4*>(o);
   const uint4* d4 = static_cast<const uint4*>(dO);
@@ -128,6 +129,8 @@ cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const vo
   else if (d == 96) fa_bwd_preprocess_kernel<96, false><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else if (d == 128 && bf16) fa_bwd_preprocess_kernel<128, true><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else if (d == 128) fa_bwd_preprocess_kernel<128, false><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
+  else if (d == 256 && bf16) fa_bwd_preprocess_kernel<256, true><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
+  else if (d == 256) fa_bwd_preprocess_kernel<256, false><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }

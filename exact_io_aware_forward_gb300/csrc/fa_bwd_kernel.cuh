@@ -67,11 +67,18 @@ namespace {
 
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000u); }
 
+// D = 256: dK and dV of 128 keys x 256 features would fill all 512 TMEM
+// columns, so each (key tile, head) is processed by NP = 2 CTAs, one per
+// 128-feature half of dK, dV and dQ (DA = 128 accumulator columns).  Both
+// recompute S^T and dP^T over all 256 features; K, V and a single Q / dO
+// stage fill shared memory.
 template <int D>
 struct BwdCfg {
   static constexpr int BKV = 128;                   // keys per CTA (MMA M)
-  static constexpr int BQ = D == 128 ? 64 : 128;    // query rows per iteration
-  static constexpr bool DQT = D == 128;             // dQ computed transposed
+  static constexpr int BQ = D == 64 ? 128 : 64;     // query rows per iteration
+  static constexpr bool DQT = D != 64;              // dQ computed transposed
+  static constexpr int DA = D == 256 ? 128 : D;     // features of dK / dV / dQ per CTA
+  static constexpr int NP = D / DA;                 // CTAs per (key tile, head)
   static constexpr int SLABS = D / 64;
   static constexpr int KV_SLAB = BKV * 128;         // 128 rows x 64 cols x 16 bit
   static constexpr int KV_TILE = SLABS * KV_SLAB;
@@ -80,10 +87,10 @@ struct BwdCfg {
   static constexpr int PT_SLAB = BKV * 128;         // 128 key rows x 64 query cols
   static constexpr int PT_TILE = (BQ / 64) * PT_SLAB;
   static constexpr int PS = 1;                      // P^T / dS^T buffers
-  static constexpr int QS = D == 128 ? 4 : 3;       // Q / dO stages
-  // d = 128: P^T and dS^T also go to TMEM (A operands of dV and dK read from
+  static constexpr int QS = D == 128 ? 4 : D == 64 ? 3 : 1;  // Q / dO stages
+  // d >= 128: P^T and dS^T also go to TMEM (A operands of dV and dK read from
   // TMEM, saving shared-memory bandwidth); dQ then has one TMEM buffer.
-  static constexpr bool PT_TMEM = D == 128;
+  static constexpr bool PT_TMEM = D != 64;
   static constexpr int DQB = PT_TMEM ? 1 : 2;       // dQ TMEM buffers
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_TILE;
@@ -106,8 +113,8 @@ struct BwdCfg {
   static constexpr uint32_t COL_PT = COL_DQ + 64 * DQB;      // P^T, 16-bit pairs (PT_TMEM)
   static constexpr uint32_t COL_DST = COL_PT + BQ / 2;       // dS^T, 16-bit pairs (PT_TMEM)
   static constexpr uint32_t COL_DV = PT_TMEM ? COL_DST + BQ / 2 : COL_DQ + 128;
-  static constexpr uint32_t COL_DK = COL_DV + D;
-  static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
+  static constexpr uint32_t COL_DK = COL_DV + DA;
+  static_assert(COL_DK + DA <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -215,8 +222,10 @@ __global__ void __launch_bounds__(640, 1)
   // float32 dQ accumulator stay in L2; within a head key tile 0 (which sees
   // every query tile under the causal mask) goes first.
   const int n_kvt = (lay.Nk + C::BKV - 1) / C::BKV;  // key tiles of the longest sequence
-  const int bh = blockIdx.x / n_kvt;
-  const int j = blockIdx.x % n_kvt;
+  const int pass = blockIdx.x % C::NP;  // feature half (D = 256), else 0
+  const int feat0 = pass * C::DA;       // first feature of dK / dV / dQ in this CTA
+  const int bh = (blockIdx.x / C::NP) / n_kvt;
+  const int j = (blockIdx.x / C::NP) % n_kvt;
   const int kv0 = j * C::BKV;
   const SeqView sv = seq_view<VARLEN>(lay, bh);
   if (!sv.ok && kv0 == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSeqlens);
@@ -317,7 +326,7 @@ __global__ void __launch_bounds__(640, 1)
     //   warp 3: dV += P^T dO, dK += dS^T Q of tile i
     if (lane == 0) {
       constexpr uint32_t kIdSdP = idesc_f16(128, BQ, BF16, false, false);   // K-major A, K-major B
-      constexpr uint32_t kIdAcc = idesc_f16(128, D, BF16, false, true);     // K-major A, MN-major B
+      constexpr uint32_t kIdAcc = idesc_f16(128, C::DA, BF16, false, true);  // K-major A, MN-major B
       constexpr uint32_t kIdDq = idesc_f16(128, 64, BF16, true, true);      // MN-major A and B
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
@@ -338,8 +347,10 @@ __global__ void __launch_bounds__(640, 1)
       auto issue_dkdv = [&](int qs, int pb, bool first) {
         const uint64_t dp = sdesc_sw128(aP + pb * C::PT_TILE, 16, 1024);
         const uint64_t dds = sdesc_sw128(aDS + pb * C::PT_TILE, 16, 1024);
-        const uint64_t ddo = sdesc_sw128(aDO + qs * C::Q_TILE, C::Q_SLAB, 1024);
-        const uint64_t dq = sdesc_sw128(aQ + qs * C::Q_TILE, C::Q_SLAB, 1024);
+        // this CTA's feature half: slabs feat0 / 64 ..
+        const uint32_t fo = (feat0 / 64) * C::Q_SLAB;
+        const uint64_t ddo = sdesc_sw128(aDO + qs * C::Q_TILE + fo, C::Q_SLAB, 1024);
+        const uint64_t dq = sdesc_sw128(aQ + qs * C::Q_TILE + fo, C::Q_SLAB, 1024);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t op = ((kk >> 2) * C::PT_SLAB + (kk & 3) * 32) >> 4;
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(640, 1)
       };
       // dQ partial -> TMEM buffer b (warp 1).
       auto issue_dq = [&](int pb, int b) {
-        const uint64_t dk0 = sdesc_sw128(aK, C::KV_SLAB, 1024);
+        const uint64_t dk0 = sdesc_sw128(aK + (feat0 / 64) * C::KV_SLAB, C::KV_SLAB, 1024);
         const uint64_t ds0 = sdesc_sw128(aDS + pb * C::PT_TILE, C::PT_SLAB, 1024);
 #pragma unroll
         for (int kk = 0; kk < C::BKV / 16; ++kk) {
@@ -565,11 +576,13 @@ __global__ void __launch_bounds__(640, 1)
       if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
       if (ok) {
         tc_fence_after();
-        uint4* dst = reinterpret_cast<uint4*>(dv) + sv.kflat(key) * (dh / 8);
+        uint4* dst = reinterpret_cast<uint4*>(dv) + sv.kflat(key) * (dh / 8) + feat0 / 8;
+        const int cols = min(C::DA, dh - feat0);  // features of this CTA that exist
         if (n_it > 0) {
-          store_rows_from_tmem<D, BF16>(lane_base + C::COL_DV, dst, key < Nk, DROP ? drop.keep_scale : 1.f, dh);
+          store_rows_from_tmem<C::DA, BF16>(lane_base + C::COL_DV, dst, key < Nk, DROP ? drop.keep_scale : 1.f,
+                                            cols);
         } else if (key < Nk) {  // no query sees this key tile (block mask, or causal with Nq < Nk): dV = 0
-          for (int q = 0; q < dh / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+          for (int q = 0; q < cols / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     }
@@ -594,12 +607,12 @@ __global__ void __launch_bounds__(640, 1)
       if (lane == 0) mbar_arrive(&dq_empty[b]);
       const int q0 = i * BQ;
       if (C::DQT) {  // lane = feature r, column = query q0 + 32g + c: one 128-byte line per warp and column
-        float* base = dq_accum + sv.qflat(q0 + 32 * g) * dh + r;
+        float* base = dq_accum + sv.qflat(q0 + 32 * g) * dh + feat0 + r;
         if (!sv.varlen && dh == D) {  // dense rows D floats apart: constant offsets
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (q0 + 32 * g + c < Nq) red_add_f32(base + c * D, v[c]);
-        } else if (r < dh) {
+        } else if (feat0 + r < dh) {
           const long long step = (long long)sv.rstride * dh;
 #pragma unroll
           for (int c = 0; c < 32; ++c)
@@ -618,11 +631,12 @@ __global__ void __launch_bounds__(640, 1)
       if (ok) {
         tc_fence_after();
         const int key = kv0 + r;
-        uint4* dst = reinterpret_cast<uint4*>(dk) + sv.kflat(key) * (dh / 8);
+        uint4* dst = reinterpret_cast<uint4*>(dk) + sv.kflat(key) * (dh / 8) + feat0 / 8;
+        const int cols = min(C::DA, dh - feat0);
         if (n_it > 0) {
-          store_rows_from_tmem<D, BF16>(lane_base + C::COL_DK, dst, key < Nk, scale, dh);
+          store_rows_from_tmem<C::DA, BF16>(lane_base + C::COL_DK, dst, key < Nk, scale, cols);
         } else if (key < Nk) {  // dK = 0 likewise
-          for (int q = 0; q < dh / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+          for (int q = 0; q < cols / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     }
@@ -643,7 +657,7 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_kv = (a.lay.Nk + C::BKV - 1) / C::BKV;
-  const long long grid = (long long)n_kv * a.BH;
+  const long long grid = (long long)n_kv * a.BH * C::NP;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dk, a.dv, a.lse,
                                                          a.delta, a.dq_accum, a.lay, a.BH, a.scale, a.scale_log2,

@@ -25,6 +25,10 @@ cudaError_t launch_backward_dkdv_varlen(int d, bool causal, bool bf16, const Bwd
   FA_BWD_CASE(128, false, true)
   FA_BWD_CASE(128, true, false)
   FA_BWD_CASE(128, true, true)
+  FA_BWD_CASE(256, false, false)
+  FA_BWD_CASE(256, false, true)
+  FA_BWD_CASE(256, true, false)
+  FA_BWD_CASE(256, true, true)
 #undef FA_BWD_CASE
   return cudaErrorInvalidValue;
 }

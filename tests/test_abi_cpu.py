@@ -157,10 +157,11 @@ def test_varlen_validation(lib):
     assert rc == 5  # workspace too small
 
 
-def test_head_dim_256_is_forward_only(lib):
+def test_head_dim_256_has_no_block_mask(lib):
     ptr = 1 << 20
-    assert lib.fa_backward_workspace_size(1, 1, 64, 256) > 0  # shape accepted ...
-    rc = lib.fa_backward(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 64, 256, 1, 0, 0.0625, ptr, 1 << 30, None)
-    assert rc == 2  # ... but the backward pass refuses it
+    assert lib.fa_backward_workspace_size(1, 1, 64, 256) == 256 + 64 * 256 * 4
     rc = lib.fa_forward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 1, 64, 256, 1, 0, 0.0625, None)
+    assert rc == 2
+    rc = lib.fa_backward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 1, 64, 256, 1, 0,
+                                     0.0625, ptr, 1 << 30, None)
     assert rc == 2
