@@ -33,7 +33,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one dK/dV launch on C4, from an ncu capture of the current
 # kernel (dram__bytes_read.sum + dram__bytes_write.sum).  Reset to None whenever that kernel
 # changes, until a new capture is taken.
-DKDV_TRAFFIC_C4 = 809710848 + 487737600
+DKDV_TRAFFIC_C4 = 810838784 + 487481088
 
 
 def load_peaks():
@@ -372,7 +372,9 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
 
     def fwd():
-        if kind == "blocksparse":
+        if kind == "dense":
+            fa.fa_forward(q, k, v, o, lse, w.causal)
+        elif kind == "blocksparse":
             fa.fa_forward_blocksparse(q, k, v, o, lse, md, w.causal)
         elif kind == "varlen":
             fa.fa_forward_varlen(q, k, v, o, lse, cu_q, cu_k, maxlen, maxlen, w.causal)
@@ -380,7 +382,9 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
             fa.fa_forward_dropout(q, k, v, o, lse, DROP_P, DROP_SEED, DROP_OFFSET, w.causal)
 
     def dkdv():
-        if kind == "blocksparse":
+        if kind == "dense":
+            fa.fa_backward_dkdv(q, k, v, do, lse, delta, acc, dk, dv, w.causal)
+        elif kind == "blocksparse":
             fa.fa_backward_dkdv_blocksparse(q, k, v, do, lse, delta, acc, dk, dv, md, w.causal)
         elif kind == "varlen":
             fa.fa_backward_dkdv_varlen(q, k, v, do, lse, delta, acc, dk, dv, cu_q, cu_k, maxlen, maxlen, w.causal)
@@ -668,7 +672,8 @@ def run_gpu(args, w, world, rank, local):
             "bwd_tflops_2p5F": round(2.5 * F / (bwd_ms * 1e-3) / 1e12, 1),
             "kernel_ms": {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
                           "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)},
-            "roofline": {"bound": "tensor", "kernel": "fa_bwd_dkdv_kernel<128,causal,bf16>",
+            "roofline": {"bound": "tensor", "kernel": f"fa_bwd_dkdv_kernel<{128 if d == 96 else d},"
+                                                      f"{'causal' if w.causal else 'non-causal'},{w.dtype}>",
                          "achieved": round(dkdv_tflops, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(dkdv_tflops / peak, 4),
                          "traffic": DKDV_TRAFFIC_C4 if w.name.startswith("C4") else None,
@@ -690,10 +695,12 @@ def run_gpu(args, w, world, rank, local):
                             "frac_of_hbm_peak": round(dgbs / float(peaks["hbm_gbs"]), 4)}
         from exact_io_aware_forward_gb300.synth import S1
         from exact_io_aware_forward_gb300.synth import V1
-        for kind, vw in (("blocksparse", S1), ("dropout", w), ("varlen", V1)):
+        from exact_io_aware_forward_gb300.synth import W96, W256
+        for key, kind, vw in (("blocksparse", "blocksparse", S1), ("dropout", "dropout", w), ("varlen", "varlen", V1),
+                              ("d96", "dense", W96), ("d256", "dense", W256)):
             sms, sparts, _, sbufs = measure_variant(dev, kind, vw, 10, 3)
             sF = variant_flops(kind, vw, sbufs[-1])
-            result[kind] = {"workload": vw.name + (f" p={DROP_P}" if kind == "dropout" else ""),
+            result[key] = {"workload": vw.name + (f" p={DROP_P}" if kind == "dropout" else ""),
                             "ms": round(sms, 4), "fwdbwd_tflops": round(2.5 * sF / (sms * 1e-3) / 1e12, 1),
                             "fwd_tflops": round(sF / (sparts[0] * 1e-3) / 1e12, 1),
                             "dkdv_frac_of_peak": round(2.5 * sF / (sparts[2] * 1e-3) / 1e12 / peak, 4)}
@@ -733,7 +740,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="C4", help="C2, C3N, C3C, C4 or C5")
+    ap.add_argument("--workload", default="C4", help="C2, C3N, C3C, C4, C5, W96 (d=96) or W256 (d=256)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--mode", default="train", choices=["train", "decode", "blocksparse", "dropout", "varlen"],
                     help="train: fwd+bwd step (the headline); decode: split-KV decoding line; "

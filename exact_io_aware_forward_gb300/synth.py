@@ -60,7 +60,11 @@ C3N = Workload("C3 fwd+bwd non-causal N=4096 d=64 bf16 K-row-scaled", 2, 16, 409
 C3C = Workload("C3 fwd+bwd causal N=4096 d=64 bf16 K-row-scaled", 2, 16, 4096, 64, "bf16", True, 2, True)
 C4 = Workload("C4 fwd+bwd causal N=8192 d=128 bf16", 2, 32, 8192, 128, "bf16", True, 3)
 C5 = Workload("C5 fwd+bwd causal N=32768 d=128 bf16", 1, 8, 32768, 128, "bf16", True, 4)
-WORKLOADS = {"C1": C1, "C2": C2, "C3N": C3N, "C3C": C3C, "C4": C4, "C5": C5}
+# The long causal training shape at the widest head dimension (same B*H*d as C4).
+W256 = Workload("W256 fwd+bwd causal N=8192 d=256 bf16", 2, 16, 8192, 256, "bf16", True, 9)
+# d = 96 at the C4 shape.
+W96 = Workload("W96 fwd+bwd causal N=8192 d=96 bf16", 2, 32, 8192, 96, "bf16", True, 10)
+WORKLOADS = {"C1": C1, "C2": C2, "C3N": C3N, "C3C": C3C, "C4": C4, "C5": C5, "W256": W256, "W96": W96}
 
 
 def attention_inputs(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int = 0,
