@@ -46,6 +46,24 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest `value` over all ranks (every rank gets it); `value` itself
+    when there is no process group.  The timing rule of the multi-GPU line: the
+    slowest rank's time is the job's time."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, work_per_rank: float, ms_slowest: float) -> float:
+    """Whole-job throughput of a weak-scaling run: every rank processes
+    `work_per_rank` units (its own heads), the job takes the slowest rank's time."""
+    return world * work_per_rank / (ms_slowest * 1e-3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -610,13 +628,10 @@ def run_gpu(args, w, world, rank, local):
     peak_mem = torch.cuda.max_memory_allocated(dev)
     total_ms = t0.elapsed_time(t1)
     parts = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps for j in range(4)]
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_step = total_ms / args.steps
     F = w.fwd_flops()
-    value = world * 2.5 * F / (ms_step * 1e-3) / 1e12
+    value = job_throughput(world, 2.5 * F, ms_step) / 1e12
 
     # End to end through the public API: pinned host inputs in, results out.
     hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
@@ -641,10 +656,7 @@ def run_gpu(args, w, world, rank, local):
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - c0) * 1e3 / e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     fa.fa_device_status()
     elem = B * H * N * d * 2
     h2d = 4 * elem
