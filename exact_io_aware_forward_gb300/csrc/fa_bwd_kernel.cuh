@@ -45,12 +45,14 @@
 // masked elementwise.  Block-sparse (SPARSE): query tiles whose 128-row
 // block does not keep this key tile are skipped as well; a key tile kept by
 // no query tile writes dK = dV = 0.
-// Dropout (DROP): the compute warps regenerate each entry's keep bit from
-// the Philox seed and offset (fa_philox.cuh), one generator call per 8 keys
-// of a query: the 8 lanes holding those keys each make the call of one
-// query and an 8 x 8 bit transpose across the lanes hands every lane the
-// bits of its own key.  The dV operand is the kept P (scaled by the keep
-// scale in the epilogue) and dS^T = P^T * (keep * scale * dP^T - D).
+// Dropout (DROP): each entry's keep bit is regenerated from the Philox seed
+// and offset (fa_philox.cuh), one generator call per 8 keys of a query: the
+// 8 lanes holding those keys each make the call of one query and an 8 x 8 bit
+// transpose across the lanes hands every lane the bits of its own key.  The
+// dQ drain warps, which share the compute warps' TMEM lanes (keys) and wait
+// for most of each tile, draw the bits one tile ahead into shared memory.
+// The dV operand is the kept P (scaled by the keep scale in the epilogue)
+// and dS^T = P^T * (keep * scale * dP^T - D).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -99,10 +101,12 @@ struct BwdCfg {
   static constexpr int OFF_P = OFF_DO + QS * Q_TILE; // [PS]
   static constexpr int OFF_DS = OFF_P + (PT_TMEM ? 0 : PS * PT_TILE);
   static constexpr int OFF_LD = OFF_DS + PS * PT_TILE;  // [2][2][BQ] floats: LSE*log2e, D
-  static constexpr int OFF_BAR = OFF_LD + 2 * 2 * BQ * 4;
+  // dropout keep words [2 buffers][2 compute warpgroups][128 keys] x uint2, drawn by the dQ drain warps
+  static constexpr int OFF_KEEP = OFF_LD + 2 * 2 * BQ * 4;
+  static constexpr int OFF_BAR = OFF_KEEP + 2 * 2 * BKV * 8;
   // kv_full, q_full[QS], q_empty[QS], sdp_full, sdp_empty, pds_full[PS], pds_empty[PS],
   // dq_full[2], dq_empty[2], ld_full[2], dkdv_full, drain[3]
-  static constexpr int NBAR = 1 + 2 * QS + 1 + 1 + 2 * PS + 2 + 2 + 2 + 1 + 3;
+  static constexpr int NBAR = 1 + 2 * QS + 1 + 1 + 2 * PS + 2 + 2 + 2 + 1 + 3 + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 640;
@@ -171,15 +175,6 @@ __device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint4* dst,
   }
 }
 
-// One step of an 8 x 8 bit-matrix transpose across the 8 lanes of a group
-// (two matrices at once, in bits 0-7 and 8-15): lane r holds row r, bit c is
-// column c; after the steps m = 4, 2, 1 lane r holds column r.
-__device__ __forceinline__ uint32_t transpose8_step(uint32_t x, int lane, int m, uint32_t lo_mask) {
-  const uint32_t y = __shfl_xor_sync(0xffffffffu, x, m);
-  const uint32_t hi_mask = lo_mask << m;
-  return (lane & m) ? ((x & hi_mask) | ((y & hi_mask) >> m)) : ((x & lo_mask) | ((y & lo_mask) << m));
-}
-
 template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(640, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -213,6 +208,9 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t* ld_full = dq_empty + 2;
   uint64_t* dkdv_full = ld_full + 2;
   uint64_t* drain = dkdv_full + 1;
+  uint64_t* keep_full = drain + 3;       // [buffer * 2 + warpgroup]
+  uint64_t* keep_empty = keep_full + 4;  // [buffer * 2 + warpgroup]
+  uint2* sKeep = reinterpret_cast<uint2*>(smem + C::OFF_KEEP);  // [buffer * 2 + warpgroup][key]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -271,6 +269,10 @@ __global__ void __launch_bounds__(640, 1)
     }
     mbar_init(dkdv_full, 1);
     for (int i = 0; i < 3; ++i) mbar_init(&drain[i], 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&keep_full[i], 4);   // the drain warpgroup that draws them
+      mbar_init(&keep_empty[i], 4);  // the compute warpgroup that uses them
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -454,35 +456,12 @@ __global__ void __launch_bounds__(640, 1)
       }
     };
     // Dropout keep bits of this thread's key for the CW query columns of the
-    // next tile (bit 16 sc + c <-> query column 16 sc + c of this warpgroup),
-    // drawn after the previous tile's P / dS are handed over, off the path
-    // from S^T to P^T.  Lane 8g + r8 draws queries c0 + r8 and c0 + 8 + r8
-    // for the 8 keys of its group; an 8 x 8 bit transpose across the group
-    // gives each lane the bits of its own key (key offset r8).
-    uint32_t kw0 = 0u, kw1 = 0u;  // columns 0-31, 32-63
-    auto draw_keep = [&](int q0n) {
-      const uint32_t kgrp = (uint32_t)(key >> 3);
-      const int r8 = lane & 7;
-#pragma unroll
-      for (int sc = 0; sc < CW / 16; ++sc) {
-        const int c0 = q0n + h * CW + 16 * sc;
-        const uint4 w0 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + r8), (uint32_t)bh, drop.offset), drop.k0,
-                                       drop.k1);
-        const uint4 w1 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + 8 + r8), (uint32_t)bh, drop.offset),
-                                       drop.k0, drop.k1);
-        uint32_t x = keep_byte(w0, drop.t) | (keep_byte(w1, drop.t) << 8);
-        x = transpose8_step(x, lane, 4, 0x0F0Fu);
-        x = transpose8_step(x, lane, 2, 0x3333u);
-        x = transpose8_step(x, lane, 1, 0x5555u);
-        if (sc == 0) kw0 = x;
-        if (sc == 1) kw0 |= x << 16;
-        if (sc == 2) kw1 = x;
-        if (sc == 3) kw1 |= x << 16;
-      }
-    };
+    // current tile (bit c of kw0 <-> query column c of this warpgroup, bit c
+    // of kw1 <-> column 32 + c), drawn one tile ahead by the dQ drain warps of
+    // the same TMEM lanes (key_keep_words in fa_philox.cuh).
+    uint32_t kw0 = 0u, kw1 = 0u;
     int i = next_tile(i_begin);
     fetch(i);
-    if (DROP && n_it > 0) draw_keep(i * BQ);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int lb = it & 1;
@@ -500,6 +479,15 @@ __global__ void __launch_bounds__(640, 1)
       i = next_tile(i + 1);
       if (it + 1 < n_it) fetch(i);
       if (!(ok = warp_wait(sdp_full, it & 1, abort_flag, status))) break;
+      if (DROP) {
+        const int kb = (it & 1) * 2 + h;
+        if (!(ok = warp_wait(&keep_full[kb], (it >> 1) & 1, abort_flag, status))) break;
+        const uint2 kw = sKeep[kb * C::BKV + r];
+        kw0 = kw.x;
+        kw1 = kw.y;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&keep_empty[kb]);
+      }
       tc_fence_after();
 #pragma unroll 1
       for (int sc = 0; sc < CW / 16; ++sc) {
@@ -570,7 +558,6 @@ __global__ void __launch_bounds__(640, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pds_full[pb]);
-      if (DROP && it + 1 < n_it) draw_keep(i * BQ);  // i is already the next tile
     }
     if (h == 0) {
       if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
@@ -595,8 +582,20 @@ __global__ void __launch_bounds__(640, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     bool ok = true;
-    for (int it = 0, i = next_tile(i_begin); it < n_it; ++it, i = next_tile(i + 1)) {
+    // Dropout keep words of tile `it` (query tile i) for compute warpgroup g:
+    // drawn here, one tile ahead, where the drain warps would otherwise wait.
+    auto draw = [&](int it, int i) {
+      const int kb = (it & 1) * 2 + g;
+      if (!warp_wait(&keep_empty[kb], ((it >> 1) & 1) ^ 1, abort_flag, status)) return false;
+      sKeep[kb * C::BKV + r] = key_keep_words(kv0 + r, i * BQ + g * (BQ / 2), BQ / 2, lane, bh, drop);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&keep_full[kb]);
+      return true;
+    };
+    if (DROP && n_it > 0) ok = draw(0, next_tile(i_begin));
+    for (int it = 0, i = next_tile(i_begin); ok && it < n_it; ++it, i = next_tile(i + 1)) {
       const int b = it % C::DQB;
+      if (DROP && it + 1 < n_it && !(ok = draw(it + 1, next_tile(i + 1)))) break;
       if (!(ok = warp_wait(&dq_full[b], (it / C::DQB) & 1, abort_flag, status))) break;
       tc_fence_after();
       float v[32];

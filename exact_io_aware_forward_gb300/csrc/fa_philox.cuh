@@ -85,4 +85,38 @@ __device__ __forceinline__ uint32_t pair_keep_mask(uint32_t eo, int i) {
   return m;
 }
 
+// Backward: the keep bits of key `key` for the `ncols` (16, 32 or 64)
+// queries q0 .. q0 + ncols - 1, bit c <-> query q0 + c (x: 0-31, y: 32-63).
+// One generator call covers 8 keys of one query, so lanes 8g .. 8g+7 (keys
+// key & ~7 .. +7) each draw the call of one query and an 8 x 8 bit transpose
+// across the group hands each lane the bits of its own key (offset lane & 7).
+// Every lane of the warp must call it with the same q0 and ncols.
+__device__ __forceinline__ uint32_t transpose8_step(uint32_t x, int lane, int m, uint32_t lo_mask) {
+  const uint32_t y = __shfl_xor_sync(0xffffffffu, x, m);
+  const uint32_t hi_mask = lo_mask << m;
+  return (lane & m) ? ((x & hi_mask) | ((y & hi_mask) >> m)) : ((x & lo_mask) | ((y & lo_mask) << m));
+}
+
+template <typename Drop>
+__device__ __forceinline__ uint2 key_keep_words(int key, int q0, int ncols, int lane, int bh, const Drop& drop) {
+  const uint32_t kgrp = (uint32_t)(key >> 3);
+  const int r8 = lane & 7;
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int sc = 0; sc < 4; ++sc) {  // 16 queries per step
+    if (16 * sc >= ncols) break;
+    const int c0 = q0 + 16 * sc;
+    const uint4 w0 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + r8), (uint32_t)bh, drop.offset), drop.k0,
+                                   drop.k1);
+    const uint4 w1 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + 8 + r8), (uint32_t)bh, drop.offset), drop.k0,
+                                   drop.k1);
+    uint32_t x = keep_byte(w0, drop.t) | (keep_byte(w1, drop.t) << 8);
+    x = transpose8_step(x, lane, 4, 0x0F0Fu);
+    x = transpose8_step(x, lane, 2, 0x3333u);
+    x = transpose8_step(x, lane, 1, 0x5555u);
+    w[sc >> 1] |= x << (16 * (sc & 1));
+  }
+  return make_uint2(w[0], w[1]);
+}
+
 }  // namespace fa
