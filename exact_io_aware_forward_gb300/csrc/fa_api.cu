@@ -486,7 +486,7 @@ namespace {
 fa_status decode_plan(int B, int H, int Nq, int Nk, int d, int num_splits, int* splits, int* chunk,
                       size_t* bytes) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   const long long BH = (long long)B * H;
   if (BH > 65535 || BH * Nk * d >= (1LL << 31) || BH * Nq * d >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > 1024) return FA_ERR_INVALID_ARG;

@@ -323,6 +323,7 @@ int decode_chunk(int Nk, int num_splits) {
 cudaError_t launch_decode(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream) {
   if (d == 64) return bf16 ? launch_decode_t<64, true>(a, stream) : launch_decode_t<64, false>(a, stream);
   if (d == 128) return bf16 ? launch_decode_t<128, true>(a, stream) : launch_decode_t<128, false>(a, stream);
+  if (d == 256) return bf16 ? launch_decode_t<256, true>(a, stream) : launch_decode_t<256, false>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -25,7 +25,8 @@
  *   16-bit type `dtype` (FA_FP16 or FA_BF16).  LSE and D are contiguous
  *   [B, H, N] float32 arrays.  LSE is in natural-log units of the scaled
  *   scores: LSE_i = ln sum_j exp(s * q_i . k_j).
- * - Supported: d in {64, 96, 128} (split-KV decoding: 64, 128); N >= 1
+ * - Supported: d in {64, 96, 128, 256} (split-KV decoding: 64, 128, 256; block masks: not
+ *   256); N >= 1
  *   (any N: tails are masked); B, H >= 1 with B*H*N*d < 2^31; scale finite
  *   and > 0.  d = 96 runs the d = 128 kernels with features 96-127 read as
  *   zero and never stored.
@@ -258,7 +259,7 @@ fa_status fa_backward_dkdv_varlen(const void* q, const void* k, const void* v, c
  * num_splits = 0 picks a count that fills the GPU; otherwise 1..1024.
  * workspace: fa_decode_workspace_size(B,H,Nq,Nk,d,num_splits) bytes of
  * device memory (partial outputs), contents irrelevant on entry.
- * Supported: d in {64, 128}, fp16/bf16, B*H <= 65535, Nq, Nk >= 1.
+ * Supported: d in {64, 128, 256}, fp16/bf16, B*H <= 65535, Nq, Nk >= 1.
  */
 size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
 fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

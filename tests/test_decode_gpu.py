@@ -42,6 +42,8 @@ CASES = [
     (1, 2, 3, 1000, 64, "bf16", True, 7), (1, 2, 4, 1000, 128, "fp16", False, 3), (2, 2, 5, 4100, 128, "bf16", True, 0),
     (1, 3, 16, 700, 64, "fp16", True, 1), (1, 2, 17, 2000, 128, "bf16", True, 9), (1, 1, 40, 40, 128, "bf16", True, 0),
     (2, 2, 40, 5000, 64, "bf16", False, 0), (1, 2, 8, 257, 128, "fp16", True, 64),
+    # head dimension 256
+    (1, 2, 1, 3000, 256, "bf16", True, 0), (1, 2, 4, 999, 256, "fp16", False, 5), (1, 1, 20, 700, 256, "bf16", True, 0),
 ]
 
 
