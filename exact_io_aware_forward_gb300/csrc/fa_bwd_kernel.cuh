@@ -1,6 +1,7 @@
 // dK / dV kernel of the backward pass on sm_103a (stage 2 of fa_backward): the
 // kernel template, shared by the translation units that instantiate it
-// (fa_bwd.cu: dense and block-sparse; fa_bwd_dropout.cu: dropout).
+// (fa_bwd.cu: dense and block-sparse; fa_bwd_dropout.cu: dropout;
+// fa_bwd_varlen.cu: packed variable-length batches).
 //
 // Math ("FlashAttention 为什么不需要存下注意力矩阵", jefxiong.cn, section 3.3):
 // with G = dO, P = exp(s Q K^T - LSE) recomputed tile by tile on chip,

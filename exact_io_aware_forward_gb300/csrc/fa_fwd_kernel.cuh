@@ -1,6 +1,7 @@
 // Forward pass of exact attention on sm_103a: the kernel template, shared by
 // the translation units that instantiate it (fa_fwd.cu: dense and
-// block-sparse; fa_fwd_dropout.cu: dropout).
+// block-sparse; fa_fwd_dropout.cu: dropout; fa_fwd_varlen.cu: packed
+// variable-length batches; fa_fwd256.cu reuses its helpers for d = 256).
 //
 // Algorithm: the online-softmax recurrence of "FlashAttention 为什么不需要存下
 // 注意力矩阵" (jefxiong.cn), section 3.2 -- per query row a reference max m, a
