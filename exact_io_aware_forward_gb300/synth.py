@@ -90,6 +90,14 @@ def attention_inputs(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: 
     return (q.to(t), k.to(t), v.to(t), None if do is None else do.to(t))
 
 
+def device_inputs(B: int, H: int, N: int, d: int, dtype: str, seed: int, device, count: int = 3):
+    """`count` tensors [B, H, N, d] drawn N(0,1) in float32 by a seeded
+    generator on `device` and rounded once to the 16-bit type; for problems
+    too large to draw on the host (the draws differ from ``attention_inputs``)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    return tuple(torch.randn(B, H, N, d, generator=g, device=device).to(DTYPES[dtype]) for _ in range(count))
+
+
 def workload_inputs(w: Workload, with_do: bool | None = None):
     """Inputs of a named workload (see ``WORKLOADS``)."""
     if with_do is None:
