@@ -347,6 +347,12 @@ def fa_forward_decode(q, k, v, o, lse, workspace, causal=False, scale=None, num_
                                                         workspace.numel(), _stream(stream)))
 
 
+def fa_selftest_wait_timeout(stream=None) -> None:
+    """Enqueue the failure-detection self-test (a bounded wait that never
+    completes; ~2 s); the next fa_device_status() raises FA_ERR_TIMEOUT."""
+    _check("fa_selftest_wait_timeout", lib().fa_selftest_wait_timeout(_stream(stream)))
+
+
 def fa_device_status(stream=None) -> None:
     """Synchronise ``stream``; raise FAError if a kernel latched a timeout."""
     _check("fa_device_status", lib().fa_device_status(_stream(stream)))

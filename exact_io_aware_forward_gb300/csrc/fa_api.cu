@@ -545,6 +545,13 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o
   return FA_OK;
 }
 
+fa_status fa_selftest_wait_timeout(void* stream) {
+  unsigned int* st = status_word();
+  if (!st) return FA_ERR_CUDA;
+  if (fa::launch_selftest_wait_timeout(st, static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 fa_status fa_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   unsigned int v = 0;

@@ -12,6 +12,7 @@
 #include <cuda_fp16.h>
 
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
 
 namespace fa {
 namespace {
@@ -105,6 +106,16 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float4* __
   }
 }
 
+// The bounded pipeline wait of every kernel, on a barrier that never completes.
+__global__ void fa_selftest_wait_kernel(unsigned int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  mbar_wait(&bar, 0, &abort_flag, status, kStatusTimeout);  // gives up after kWaitTimeoutNs
+}
+
 int grid_for(long long threads_needed) {
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -132,6 +143,11 @@ cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const vo
   else if (d == 256 && bf16) fa_bwd_preprocess_kernel<256, true><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else if (d == 256) fa_bwd_preprocess_kernel<256, false><<<grid, 256, 0, stream>>>(o4, d4, delta, acc, rows);
   else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait_timeout(unsigned int* status, cudaStream_t stream) {
+  fa_selftest_wait_kernel<<<1, 1, 0, stream>>>(status);
   return cudaGetLastError();
 }
 

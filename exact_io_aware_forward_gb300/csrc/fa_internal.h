@@ -90,6 +90,9 @@ cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const vo
                                        float* dq_accum, long long rows, cudaStream_t stream);
 cudaError_t launch_backward_dq_convert(int d, bool bf16, const float* dq_accum, void* dq, long long rows,
                                        float scale, cudaStream_t stream);
+// One thread waits, with the kernels' bounded wait, on an mbarrier that no
+// one arrives at; the wait gives up and latches kStatusTimeout in *status.
+cudaError_t launch_selftest_wait_timeout(unsigned int* status, cudaStream_t stream);
 
 struct DecodeArgs {
   const void* q;       // [B*H, Nq, d]

@@ -168,6 +168,16 @@ fa_status fa_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, float p_dr
                                void* stream);
 
 /*
+ * Self-test of failure detection: launches one thread that waits, with the
+ * bounded pipeline wait every kernel uses, on a barrier nothing ever
+ * completes.  The wait gives up after ~2 s and latches FA_ERR_TIMEOUT, so the
+ * next fa_device_status() returns FA_ERR_TIMEOUT (and clears it) while the
+ * context stays usable.  No counterpart in the pages: it checks that a stuck
+ * pipeline ends and is reported instead of hanging the GPU.
+ */
+fa_status fa_selftest_wait_timeout(void* stream);
+
+/*
  * Stage 1 of the backward pass: D_i = sum_c dO_ic * O_ic in float32 (the
  * row-sum shortcut for rowsum(P * (dO V^T)), which holds because O = P V),
  * and dq_accum := 0.  delta: [B,H,N] float32 out; dq_accum: [B,H,N,d]
