@@ -68,7 +68,8 @@ def _check(q, k, v, do, bm, causal, o, lse, dq, dk, dv, dtype):
 
 @pytest.mark.parametrize("per_head", [False, True])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N,d,dtype", [(300, 64, "fp16"), (640, 128, "bf16"), (1000, 64, "bf16"), (513, 128, "fp16")])
+@pytest.mark.parametrize("N,d,dtype", [(300, 64, "fp16"), (640, 128, "bf16"), (1000, 64, "bf16"), (513, 128, "fp16"),
+                                       (700, 96, "bf16")])
 def test_blocksparse_matches_oracle(per_head, causal, N, d, dtype):
     B, H = 1, 3
     q, k, v, do = attention_inputs(B, H, N, d, dtype, seed=3000 + N + d)

@@ -87,7 +87,7 @@ def _check(q, k, v, do, causal, p, seed, offset, o, lse, dq, dk, dv, dtype):
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N,d,dtype,p", [(300, 64, "fp16", 0.1), (640, 128, "bf16", 0.2), (1000, 64, "bf16", 0.5),
-                                         (513, 128, "fp16", 0.15), (1, 64, "bf16", 0.3)])
+                                         (513, 128, "fp16", 0.15), (1, 64, "bf16", 0.3), (450, 96, "bf16", 0.25)])
 def test_dropout_matches_oracle(causal, N, d, dtype, p):
     B, H = 1, 3
     q, k, v, do = attention_inputs(B, H, N, d, dtype, seed=5000 + N + d)

@@ -35,7 +35,9 @@ def test_rejects_problems_beyond_the_scratch():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("B,H,N,d,dtype,causal", [(1, 4, 1000, 128, "bf16", True),
-                                                   (2, 3, 515, 64, "fp16", False)])
+                                                   (2, 3, 515, 64, "fp16", False),
+                                                   (1, 2, 600, 96, "bf16", True),
+                                                   (1, 2, 400, 256, "bf16", True)])
 def test_noalloc_matches_workspace_backward(B, H, N, d, dtype, causal):
     dev = torch.device("cuda:0")
     q, k, v, do = (x.to(dev) for x in attention_inputs(B, H, N, d, dtype, seed=4242 + N))
