@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(640, 1)
                        void* __restrict__ dk, void* __restrict__ dv, const float* __restrict__ lse,
                        const float* __restrict__ delta, float* __restrict__ dq_accum, SeqLayout lay, int BH,
                        float scale, float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads,
-                       DropParams drop, unsigned int* status) {
+                       DropParams drop, int group, unsigned int* status) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
   constexpr float kLog2e = 1.4426950408889634f;
@@ -217,14 +217,21 @@ __global__ void __launch_bounds__(640, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Head-major order: the CTAs of one head run together, so its Q, dO and
-  // float32 dQ accumulator stay in L2; within a head key tile 0 (which sees
-  // every query tile under the causal mask) goes first.
+  // Heads are taken in groups of `group` (chosen by the launcher so that a
+  // group's Q, dO and float32 dQ accumulators fit in about half of L2): the
+  // CTAs of a group run together, and inside a group key tile 0 of every head
+  // (which sees every query tile under the causal mask) goes first, then key
+  // tile 1, ...: the longest CTAs start early instead of at the end.
+  const int kGroup = group;
   const int n_kvt = (lay.Nk + C::BKV - 1) / C::BKV;  // key tiles of the longest sequence
   const int pass = blockIdx.x % C::NP;  // feature half (D = 256), else 0
   const int feat0 = pass * C::DA;       // first feature of dK / dV / dQ in this CTA
-  const int bh = (blockIdx.x / C::NP) / n_kvt;
-  const int j = (blockIdx.x / C::NP) % n_kvt;
+  const int cta = blockIdx.x / C::NP;
+  const int gi = cta / (kGroup * n_kvt);
+  const int heads = min(kGroup, BH - gi * kGroup);  // the last group may be smaller
+  const int within = cta - gi * kGroup * n_kvt;
+  const int bh = gi * kGroup + within % heads;
+  const int j = within / heads;
   const int kv0 = j * C::BKV;
   const SeqView sv = seq_view<VARLEN>(lay, bh);
   if (!sv.ok && kv0 == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSeqlens);
@@ -650,6 +657,16 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
+// Heads per CTA group: Q and dO (16-bit) and the float32 dQ accumulator of a
+// head take 8 * Nq * d bytes; a group keeps them within ~64 MB of L2.
+inline int heads_per_group(const BwdArgs& a, int D) {
+  const long long per_head = 8LL * a.lay.Nq * D;
+  long long g = (64LL << 20) / (per_head > 0 ? per_head : 1);
+  if (g > 16) g = 16;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
 template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
@@ -661,7 +678,8 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dk, a.dv, a.lse,
                                                          a.delta, a.dq_accum, a.lay, a.BH, a.scale, a.scale_log2,
-                                                         a.block_mask, a.mask_heads, a.drop, a.status);
+                                                         a.block_mask, a.mask_heads, a.drop, heads_per_group(a, D),
+                                                         a.status);
   return cudaGetLastError();
 }
 
