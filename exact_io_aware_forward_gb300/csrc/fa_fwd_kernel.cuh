@@ -50,6 +50,8 @@
 // multiplied by the keep scale 1 / (1 - t / 65536) in the epilogue.
 #pragma once
 
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o,
                   float* __restrict__ lse, SeqLayout lay, int BH, int n_qblocks, float scale_log2,
-                  const uint8_t* __restrict__ block_mask, int mask_heads, DropParams drop,
+                  const uint8_t* __restrict__ block_mask, int mask_heads, DropParams drop, int group,
                   unsigned int* status) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -153,9 +155,14 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Heaviest work first: the last query blocks see the most keys under the mask.
-  const int bh = blockIdx.x % BH;
-  const int qb = n_qblocks - 1 - blockIdx.x / BH;
+  // Heads in groups of `group` (a group's K and V fit in about half of L2);
+  // inside a group the heaviest work first: under the causal mask the last
+  // query blocks see the most keys.
+  const int gi = blockIdx.x / (group * n_qblocks);
+  const int heads = min(group, BH - gi * group);  // the last group may be smaller
+  const int within = blockIdx.x - gi * group * n_qblocks;
+  const int bh = gi * group + within % heads;
+  const int qb = n_qblocks - 1 - within / heads;
   const int q0 = qb * (C::QT * C::BM);
   const SeqView sv = seq_view<VARLEN>(lay, bh);
   if (!sv.ok && q0 == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSeqlens);
@@ -572,8 +579,11 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   const int n_qblocks = (a.lay.Nq + C::QT * C::BM - 1) / (C::QT * C::BM);
   const long long grid = (long long)n_qblocks * a.BH;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // K and V of a head take 4 * Nk * D bytes; a group keeps them within ~64 MB of L2.
+  const long long per_head = 4LL * a.lay.Nk * D;
+  const int group = (int)std::max(1LL, std::min(64LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.lay, a.BH, n_qblocks,
-                                                         a.scale_log2, a.block_mask, a.mask_heads, a.drop,
+                                                         a.scale_log2, a.block_mask, a.mask_heads, a.drop, group,
                                                          a.status);
   return cudaGetLastError();
 }
