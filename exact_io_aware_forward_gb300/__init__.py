@@ -12,4 +12,4 @@ from .api import (FAError, backward, fa_backward, fa_backward_dkdv, fa_backward_
                   fa_forward_varlen, fa_backward_varlen, fa_backward_varlen_workspace_size, forward_varlen,
                   backward_varlen, fa_backward_dkdv_varlen, fa_selftest_wait_timeout,
                   fa_backward_preprocess, fa_backward_workspace_size, fa_device_status, fa_forward,
-                  forward)
+                  fa_score_blocks, forward)

@@ -50,6 +50,7 @@ SIGNATURES = {
                                      _I, _F, _F, _U64, _U32, _P]),
     "fa_selftest_wait_timeout": (_I, [_P]),
     "fa_device_status": (_I, [_P]),
+    "fa_score_blocks": (_I, [_P, ctypes.POINTER(_U64), ctypes.POINTER(_U64), _I]),
 }
 
 _lock = threading.Lock()

@@ -9,6 +9,7 @@ with torch.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 
 import torch
@@ -356,6 +357,15 @@ def fa_selftest_wait_timeout(stream=None) -> None:
 def fa_device_status(stream=None) -> None:
     """Synchronise ``stream``; raise FAError if a kernel latched a timeout."""
     _check("fa_device_status", lib().fa_device_status(_stream(stream)))
+
+
+def fa_score_blocks(reset=False, stream=None):
+    """Synchronise ``stream``; return (forward, backward) counts of the 64 x 64
+    score blocks the kernels computed since the last reset (and reset them
+    if ``reset``)."""
+    f, b = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check("fa_score_blocks", lib().fa_score_blocks(_stream(stream), ctypes.byref(f), ctypes.byref(b), int(bool(reset))))
+    return f.value, b.value
 
 
 # ---------------------------------------------------------------- conveniences

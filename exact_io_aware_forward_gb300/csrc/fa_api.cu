@@ -10,8 +10,9 @@
 
 namespace {
 
-// Device status word: kernels OR fa::kStatus* bits into it.
-__device__ unsigned int g_fa_status;
+// Device status block: kernels OR fa::kStatus* bits into word 0 and add to the
+// score-block counters behind it (layout in fa_internal.h).
+__device__ __align__(16) unsigned int g_fa_status[fa::kStatusWords];
 
 unsigned int* status_word() {
   void* p = nullptr;
@@ -561,6 +562,20 @@ fa_status fa_device_status(void* stream) {
     if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
     if (v & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
     if (v & fa::kStatusBadSeqlens) return FA_ERR_SEQLENS;
+  }
+  return FA_OK;
+}
+
+fa_status fa_score_blocks(void* stream, unsigned long long* fwd_blocks, unsigned long long* bwd_blocks, int reset) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned long long c[2] = {0ull, 0ull};
+  if (cudaMemcpyFromSymbol(c, g_fa_status, sizeof(c), 2 * sizeof(unsigned int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (fwd_blocks) *fwd_blocks = c[fa::kCountForward];
+  if (bwd_blocks) *bwd_blocks = c[fa::kCountBackward];
+  if (reset) {
+    const unsigned long long zero[2] = {0ull, 0ull};
+    if (cudaMemcpyToSymbol(g_fa_status, zero, sizeof(zero), 2 * sizeof(unsigned int)) != cudaSuccess)
+      return FA_ERR_CUDA;
   }
   return FA_OK;
 }

@@ -427,7 +427,11 @@ __global__ void __launch_bounds__(640, 1)
           mma_commit(&q_empty[qs]);
         }
       }
-      if (ok && warp == 3) mma_commit(dkdv_full);
+      if (ok && warp == 3) {
+        mma_commit(dkdv_full);
+        // score blocks of this key tile (counted once, by feature half 0)
+        if (pass == 0) count_score_blocks(status, kCountBackward, (unsigned long long)n_it * (C::BKV / 64) * (BQ / 64));
+      }
       if (!ok) {  // every MMA this thread issued must finish before TMEM is freed
         mma_commit(&drain[warp - 1]);
         drain_wait(&drain[warp - 1], 0);

@@ -231,6 +231,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       mma_commit(ok ? o_full : drain);  // with no key tile this arrives at once
+      if (ok) count_score_blocks(status, kCountForward, (unsigned long long)n * (C::BN / 32));  // 128 x BN each
       if (!ok) drain_wait(drain, 0);    // every MMA issued must finish before TMEM is freed
     }
   } else {

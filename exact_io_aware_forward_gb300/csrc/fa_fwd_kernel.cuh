@@ -338,6 +338,10 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) issue_pv(1, jl, jl == 0);
           }
         }
+        // Both query tiles run every key tile they see, query tile 1 also when
+        // it starts past the last row (an odd number of query tiles): its
+        // scores are computed and its rows never stored.
+        if (ok) count_score_blocks(status, kCountForward, 4ull * (unsigned)(n0 + n1));
       } else {
         // Per load-order position u: PV_0(prev), S_0(u), PV_1(prev), S_1(u), where
         // prev is the previous position; a query tile skips the products of the
@@ -393,6 +397,7 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) issue_pv(1, prev, c1 == 1);
           }
         }
+        if (ok) count_score_blocks(status, kCountForward, 4ull * (unsigned)(c0 + c1));
       }
       if (ok) mma_commit(o_full);
       if (!ok) {  // every MMA issued so far must finish before TMEM is freed

@@ -12,6 +12,20 @@ namespace fa {
 constexpr unsigned int kStatusTimeout = 1u;
 constexpr unsigned int kStatusBadSeqlens = 2u;  // a cu_seqlens range outside the packed tensors or maxima
 
+// The device status block: word 0 holds the kStatus* bits; words 2-3 and 4-5
+// are two 64-bit counters of the 64 x 64 (query x key) score blocks that the
+// forward and the backward kernels computed.  Kernels get a pointer to word 0.
+constexpr int kStatusWords = 6;
+constexpr int kCountForward = 0;
+constexpr int kCountBackward = 1;
+
+#ifdef __CUDACC__
+// Adds n score blocks to counter `which` (kCountForward / kCountBackward).
+__device__ __forceinline__ void count_score_blocks(unsigned int* status, int which, unsigned long long n) {
+  atomicAdd(reinterpret_cast<unsigned long long*>(status + 2) + which, n);
+}
+#endif
+
 // Where the rows of each (sequence, head) problem live.
 //   dense  (cu_q == nullptr): q/o/dq [B, H, Nq, dh], k/v/dk/dv [B, H, Nk, dh]
 //          head-major, every sequence of the same length; lse/delta [B, H, Nq].

@@ -309,6 +309,24 @@ fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const
  */
 fa_status fa_device_status(void* stream);
 
+/*
+ * Work counters, for checking which score tiles the kernels compute.  The
+ * tiled algorithm (Tri Dao's FlashAttention notes, section 04.5 "Causal
+ * Masking": a tile lying wholly above the diagonal is skipped) visits
+ * T(T+1)/2 of the T x T square tiles under the causal mask, and the
+ * block-sparse variant only the kept blocks.  Every forward and dK/dV kernel
+ * adds the score blocks it computed, in units of 64 query rows x 64 keys
+ * (a 128 x 128 tile counts 4), to one of two 64-bit device counters: the
+ * forward kernels to *fwd_blocks, the dK/dV kernels to *bwd_blocks (a
+ * score block recomputed by both feature halves at d = 256 counts once).
+ * Tiles cover whole tile shapes, so at a ragged tail a partial tile counts
+ * in full.  Waits for all work queued on `stream`, stores both counters
+ * through the host pointers (either may be NULL) and zeroes them if `reset`
+ * is nonzero.  Blocks the host.  Errors: FA_ERR_CUDA if the stream or a copy
+ * fails.
+ */
+fa_status fa_score_blocks(void* stream, unsigned long long* fwd_blocks, unsigned long long* bwd_blocks, int reset);
+
 #ifdef __cplusplus
 }
 #endif
