@@ -144,15 +144,15 @@ bool make_map(CUtensorMap* m, const void* ptr, const Shape& s, bool key_side, in
   return r == CUDA_SUCCESS;
 }
 
-// Dropout probability -> generator parameters: t = round(p * 65536), keep
-// scale 65536 / (65536 - t).  False for p outside [0, 1) (NaN included) or
-// p rounding to 1.
+// Dropout probability -> generator parameters: t = round(p * 256), keep
+// scale 256 / (256 - t).  False for p outside [0, 1) (NaN included) or p
+// rounding to 1.
 bool make_drop(float p, uint64_t seed, uint32_t offset, fa::DropParams* dp) {
   if (!(p >= 0.f && p < 1.f)) return false;
-  const double t = floor((double)p * 65536.0 + 0.5);
-  if (t >= 65536.0) return false;
+  const double t = floor((double)p * 256.0 + 0.5);
+  if (t >= 256.0) return false;
   dp->t = (uint32_t)t;
-  dp->keep_scale = (float)(65536.0 / (65536.0 - t));
+  dp->keep_scale = (float)(256.0 / (256.0 - t));
   dp->k0 = (uint32_t)(seed & 0xffffffffu);
   dp->k1 = (uint32_t)(seed >> 32);
   dp->offset = offset;

@@ -6,9 +6,9 @@
 namespace fa {
 namespace {
 
-// One thread per 8 keys of one query row: one generator call.
+// One thread per 16 keys of one query row: one generator call.
 __global__ void fa_dropout_keep_mask_kernel(uint8_t* __restrict__ keep, int BH, int Nq, int Nk, DropParams drop) {
-  const int groups = (Nk + 7) / 8;
+  const int groups = (Nk + 15) / 16;
   const long long total = (long long)BH * Nq * groups;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -17,9 +17,9 @@ __global__ void fa_dropout_keep_mask_kernel(uint8_t* __restrict__ keep, int BH, 
     const int i = (int)(rowid % Nq);
     const int bh = (int)(rowid / Nq);
     const uint4 w = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)i, (uint32_t)bh, drop.offset), drop.k0, drop.k1);
-    const uint32_t bits = keep_byte(w, drop.t);
-    uint8_t* dst = keep + rowid * Nk + 8LL * g;
-    for (int k = 0; k < 8 && 8 * g + k < Nk; ++k) dst[k] = (uint8_t)((bits >> k) & 1u);
+    const uint32_t bits = keep_bits16(w, drop.t * 0x01010101u);
+    uint8_t* dst = keep + rowid * Nk + 16LL * g;
+    for (int k = 0; k < 16 && 16 * g + k < Nk; ++k) dst[k] = (uint8_t)((bits >> k) & 1u);
   }
 }
 
@@ -46,7 +46,7 @@ cudaError_t launch_backward_dkdv_dropout(int d, bool causal, bool bf16, const Bw
 
 cudaError_t launch_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, const DropParams& drop,
                                      cudaStream_t stream) {
-  const long long total = (long long)BH * Nq * ((Nk + 7) / 8);
+  const long long total = (long long)BH * Nq * ((Nk + 15) / 16);
   if (total <= 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);

@@ -47,7 +47,7 @@
 // Dropout (DROP): the softmax warps draw each entry's keep bit from the
 // Philox generator (fa_philox.cuh) and zero the dropped P entries before
 // they reach the PV product; l and LSE use the undropped P, and O is
-// multiplied by the keep scale 1 / (1 - t / 65536) in the epilogue.
+// multiplied by the keep scale 1 / (1 - t / 256) in the epilogue.
 #pragma once
 
 #include <algorithm>

@@ -45,8 +45,8 @@ struct SeqLayout {
   int dh = 0;
 };
 
-// Dropout parameters (see fa_philox.cuh): entries whose 16-bit draw is below
-// t are dropped; kept ones are scaled by keep_scale = 65536 / (65536 - t).
+// Dropout parameters (see fa_philox.cuh): entries whose 8-bit draw is below
+// t are dropped; kept ones are scaled by keep_scale = 256 / (256 - t).
 struct DropParams {
   uint32_t t = 0;
   float keep_scale = 1.f;

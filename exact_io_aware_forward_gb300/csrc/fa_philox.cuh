@@ -5,11 +5,11 @@
 // only the generator's seed and offset: the backward pass draws the same
 // keep mask again instead of reading a stored one.
 //
-// Counter mapping (one call per 8 consecutive keys of one query row):
-// entry (head bh, query i, key j) uses counter (j / 8, i, bh, offset) under
-// key (seed low word, seed high word); output word (j / 2) % 4 holds the
-// 16-bit draw of key j in its low half (j even) or high half (j odd); the
-// entry is kept iff draw >= t, with t = round(p * 65536).
+// Counter mapping (one call per 16 consecutive keys of one query row):
+// entry (head bh, query i, key j) uses counter (j / 16, i, bh, offset) under
+// key (seed low word, seed high word); output word (j / 4) % 4 holds the
+// 8-bit draw of key j in its byte j % 4 (least significant first); the entry
+// is kept iff draw >= t, with t = round(p * 256).
 #pragma once
 
 #include <stdint.h>
@@ -35,41 +35,45 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Keep bits of the 8 keys of one generator call: bit k <-> key 8 * (j / 8) + k.
-// __vsetgeu2 gives 1 in each 16-bit half whose draw is >= t.
-__device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t t) {
-  const uint32_t tt = t | (t << 16);
+// Keep bits of the 16 keys of one generator call: bit k <-> key 16 * (j / 16) + k.
+// `tt` is t in each of the four bytes; __vsetgeu4 gives 1 in bit 0 of each
+// byte whose draw is >= t, and the shifts gather those four bits.
+__device__ __forceinline__ uint32_t keep_bits16(uint4 w, uint32_t tt) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
   uint32_t b = 0;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    const uint32_t v = __vsetgeu2(ws[r], tt);
-    b |= ((v & 1u) | ((v >> 15) & 2u)) << (2 * r);
+    const uint32_t v = __vsetgeu4(ws[r], tt);
+    b |= ((v | (v >> 7) | (v >> 14) | (v >> 21)) & 0xFu) << (4 * r);
   }
   return b;
 }
 
 // Keep bits of the 32 * NW keys [kbase, kbase + 32 NW) of query `row`, one
 // word per 32 keys: in word cc, bit i is the even key kbase + 32cc + 2i of
-// pair i and bit 16 + i the odd key kbase + 32cc + 2i + 1 (4 NW generator
-// calls).
+// pair i and bit 16 + i the odd key kbase + 32cc + 2i + 1 (2 NW generator
+// calls; kbase a multiple of 32).
 template <int NW>
 __device__ __forceinline__ void tile_keep_bits(uint32_t (&eo)[NW], int kbase, int row, int bh, uint32_t offset,
                                                uint32_t k0, uint32_t k1, uint32_t t) {
-  const uint32_t tt = t | (t << 16);
+  const uint32_t tt = t * 0x01010101u;
 #pragma unroll
   for (int cc = 0; cc < NW; ++cc) {
     uint32_t e = 0;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 2; ++g) {
       const uint4 w = philox4x32_10(
-          make_uint4(((uint32_t)(kbase + 32 * cc) >> 3) + g, (uint32_t)row, (uint32_t)bh, offset), k0, k1);
-      // __vsetgeu2: 1 in each 16-bit half whose draw is >= t, i.e. bit 0 (even
-      // key) and bit 16 (odd key) of the pair held by word r.
-      e |= __vsetgeu2(w.x, tt) << (4 * g + 0);
-      e |= __vsetgeu2(w.y, tt) << (4 * g + 1);
-      e |= __vsetgeu2(w.z, tt) << (4 * g + 2);
-      e |= __vsetgeu2(w.w, tt) << (4 * g + 3);
+          make_uint4(((uint32_t)(kbase + 32 * cc) >> 4) + g, (uint32_t)row, (uint32_t)bh, offset), k0, k1);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        // Word r holds keys 16g + 4r + {0, 1, 2, 3}: the even and odd keys of
+        // pairs 8g + 2r and 8g + 2r + 1.  With v's bits at 0, 8, 16, 24, u has
+        // key +0 at bit 0, key +2 at bit 1, key +1 at bit 8, key +3 at bit 9.
+        const uint32_t v = __vsetgeu4(ws[r], tt);
+        const uint32_t u = v | (v >> 15);
+        e |= ((u & 0x3u) | ((u & 0x300u) << 8)) << (8 * g + 2 * r);
+      }
     }
     eo[cc] = e;
   }
@@ -85,35 +89,38 @@ __device__ __forceinline__ uint32_t pair_keep_mask(uint32_t eo, int i) {
   return m;
 }
 
-// Backward: the keep bits of key `key` for the `ncols` (16, 32 or 64)
-// queries q0 .. q0 + ncols - 1, bit c <-> query q0 + c (x: 0-31, y: 32-63).
-// One generator call covers 8 keys of one query, so lanes 8g .. 8g+7 (keys
-// key & ~7 .. +7) each draw the call of one query and an 8 x 8 bit transpose
-// across the group hands each lane the bits of its own key (offset lane & 7).
-// Every lane of the warp must call it with the same q0 and ncols.
-__device__ __forceinline__ uint32_t transpose8_step(uint32_t x, int lane, int m, uint32_t lo_mask) {
+// One step of a bit-matrix transpose across lanes: rows are lanes, columns
+// are bits; partners lane ^ m swap the off-diagonal m x m blocks (lo_mask
+// selects the low block of every 2m-bit group).
+__device__ __forceinline__ uint32_t transpose_step(uint32_t x, int lane, int m, uint32_t lo_mask) {
   const uint32_t y = __shfl_xor_sync(0xffffffffu, x, m);
   const uint32_t hi_mask = lo_mask << m;
   return (lane & m) ? ((x & hi_mask) | ((y & hi_mask) >> m)) : ((x & lo_mask) | ((y & lo_mask) << m));
 }
 
+// Backward: the keep bits of key `key` for the `ncols` (16, 32 or 64)
+// queries q0 .. q0 + ncols - 1, bit c <-> query q0 + c (x: 0-31, y: 32-63).
+// One generator call covers 16 keys of one query, so lanes 16h .. 16h+15
+// (keys key & ~15 .. +15) each draw the call of one query and a 16 x 16 bit
+// transpose across the half-warp hands each lane the bits of its own key
+// (key & 15 == lane & 15).  Every lane of the warp must call it with the
+// same q0 and ncols.
 template <typename Drop>
 __device__ __forceinline__ uint2 key_keep_words(int key, int q0, int ncols, int lane, int bh, const Drop& drop) {
-  const uint32_t kgrp = (uint32_t)(key >> 3);
-  const int r8 = lane & 7;
+  const uint32_t kgrp = (uint32_t)(key >> 4);
+  const int r16 = lane & 15;
+  const uint32_t tt = drop.t * 0x01010101u;
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
   for (int sc = 0; sc < 4; ++sc) {  // 16 queries per step
     if (16 * sc >= ncols) break;
-    const int c0 = q0 + 16 * sc;
-    const uint4 w0 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + r8), (uint32_t)bh, drop.offset), drop.k0,
-                                   drop.k1);
-    const uint4 w1 = philox4x32_10(make_uint4(kgrp, (uint32_t)(c0 + 8 + r8), (uint32_t)bh, drop.offset), drop.k0,
-                                   drop.k1);
-    uint32_t x = keep_byte(w0, drop.t) | (keep_byte(w1, drop.t) << 8);
-    x = transpose8_step(x, lane, 4, 0x0F0Fu);
-    x = transpose8_step(x, lane, 2, 0x3333u);
-    x = transpose8_step(x, lane, 1, 0x5555u);
+    const uint4 g = philox4x32_10(make_uint4(kgrp, (uint32_t)(q0 + 16 * sc + r16), (uint32_t)bh, drop.offset),
+                                  drop.k0, drop.k1);
+    uint32_t x = keep_bits16(g, tt);  // row: query q0 + 16 sc + r16; bit k: key 16 kgrp + k
+    x = transpose_step(x, lane, 8, 0x00FFu);
+    x = transpose_step(x, lane, 4, 0x0F0Fu);
+    x = transpose_step(x, lane, 2, 0x3333u);
+    x = transpose_step(x, lane, 1, 0x5555u);
     w[sc >> 1] |= x << (16 * (sc & 1));
   }
   return make_uint2(w[0], w[1]);

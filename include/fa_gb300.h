@@ -134,13 +134,13 @@ fa_status fa_backward_blocksparse(const void* q, const void* k, const void* v, c
  * counter-based generator, and the backward pass regenerates the mask).
  *
  * The dropout acts on the normalised probabilities: O = (P * Z / (1 - p')) V
- * with Z the keep mask and p' = t / 65536, t = round(p_drop * 65536) (p_drop
- * is quantised to 2^-16); lse is still the log-sum-exp of the undropped
- * scores.  Z is drawn with Philox4x32-10 (Salmon et al., SC 2011): entry
- * (head bh = b*H + h, query i, key j) uses counter (j / 8, i, bh, offset)
- * and key (seed & 0xffffffff, seed >> 32); word (j / 2) % 4 of the output
- * gives a 16-bit draw (low half for even j, high half for odd j), and the
- * entry is kept iff draw >= t.  The same (p_drop, seed, offset) must be
+ * with Z the keep mask and p' = t / 256, t = round(p_drop * 256) (p_drop is
+ * quantised to 2^-8); lse is still the log-sum-exp of the undropped scores.
+ * Z is drawn with Philox4x32-10 (Salmon et al., SC 2011): entry (head
+ * bh = b*H + h, query i, key j) uses counter (j / 16, i, bh, offset) and key
+ * (seed & 0xffffffff, seed >> 32); byte j % 4 (least significant first) of
+ * word (j / 4) % 4 of the output gives an 8-bit draw, and the entry is kept
+ * iff draw >= t.  The same (p_drop, seed, offset) must be
  * passed to the backward call; a new offset (or seed) gives a new mask.
  * p_drop must be in [0, 1) and not round to 1, else FA_ERR_INVALID_ARG;
  * p_drop rounding to 0 computes plain attention.  Dense attention only

@@ -22,14 +22,18 @@ The pages fix neither how counters map to attention entries nor how random
 bits become keep decisions.  The reading taken here:
 
 * entry (head bh, query row i, key column j) uses the counter
-  (j // 8, i, bh, offset) under the key (seed mod 2^32, seed div 2^32);
+  (j // 16, i, bh, offset) under the key (seed mod 2^32, seed div 2^32);
   bh = b * H + h;
-* the four 32-bit output words give eight 16-bit integers, word (j // 2) % 4
-  and its low half for even j, high half for odd j;
-* the entry is kept iff that integer is >= t, with t = round(p * 65536)
-  (so the drop probability is t / 65536, p quantised to 2^-16); kept
-  probabilities are multiplied by 65536 / (65536 - t), the inverse of the
-  keep probability, so that the expected output equals the plain output.
+* the four 32-bit output words give sixteen 8-bit integers: word (j // 4) % 4
+  and its byte j % 4, counted from the least significant byte;
+* the entry is kept iff that integer is >= t, with t = round(p * 256) (so
+  the drop probability is t / 256, p quantised to 2^-8); kept probabilities
+  are multiplied by 256 / (256 - t), the inverse of the keep probability, so
+  that the expected output equals the plain output.
+
+One generator call thus serves sixteen entries of a row; the coarser
+quantisation of p (the realised drop probability of p = 0.1 is 26/256) is
+the price of half the generator work per entry.
 
 Dropout acts on the normalised probabilities P (after the softmax); LSE is
 the softmax normaliser and is not affected.
@@ -69,37 +73,37 @@ def philox4x32_10(counters, key):
 
 
 def threshold(p: float) -> int:
-    """t = round(p * 65536); entries whose 16-bit draw is below t are dropped."""
+    """t = round(p * 256); entries whose 8-bit draw is below t are dropped."""
     if not (0.0 <= p < 1.0):
         raise ValueError("dropout probability must be in [0, 1)")
-    t = int(np.floor(p * 65536.0 + 0.5))
-    if t >= 65536:
+    t = int(np.floor(p * 256.0 + 0.5))
+    if t >= 256:
         raise ValueError("dropout probability rounds to 1")
     return t
 
 
 def keep_scale(p: float) -> float:
-    """1 / keep probability = 65536 / (65536 - t)."""
-    return 65536.0 / (65536.0 - threshold(p))
+    """1 / keep probability = 256 / (256 - t)."""
+    return 256.0 / (256.0 - threshold(p))
 
 
-def draws16(seed: int, offset: int, bh: int, rows, n_keys: int):
-    """The 16-bit draws of head ``bh`` for query rows ``rows`` and keys
-    0 .. n_keys-1: uint32 array [len(rows), n_keys] with values < 65536."""
+def draws8(seed: int, offset: int, bh: int, rows, n_keys: int):
+    """The 8-bit draws of head ``bh`` for query rows ``rows`` and keys
+    0 .. n_keys-1: uint32 array [len(rows), n_keys] with values < 256."""
     rows = np.asarray(rows, dtype=np.int64)
-    n_groups = (n_keys + 7) // 8
+    n_groups = (n_keys + 15) // 16
     ctr = np.empty((len(rows), n_groups, 4), dtype=np.uint64)
     ctr[..., 0] = np.arange(n_groups, dtype=np.uint64)[None, :]
     ctr[..., 1] = rows.astype(np.uint64)[:, None]
     ctr[..., 2] = np.uint64(bh)
     ctr[..., 3] = np.uint64(offset & 0xFFFFFFFF)
     words = philox4x32_10(ctr, (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))  # [rows, groups, 4]
-    halves = np.stack([words & 0xFFFF, words >> 16], axis=-1)  # [rows, groups, 4, 2]
-    return halves.reshape(len(rows), n_groups * 8)[:, :n_keys]
+    octets = np.stack([(words >> (8 * b)) & 0xFF for b in range(4)], axis=-1)  # [rows, groups, 4, 4]
+    return octets.reshape(len(rows), n_groups * 16)[:, :n_keys]
 
 
 def keep_mask(seed: int, offset: int, p: float, bh: int, n_queries: int, n_keys: int, rows=None):
     """Boolean keep mask [rows, n_keys] of head ``bh`` (all rows if None)."""
     if rows is None:
         rows = np.arange(n_queries)
-    return draws16(seed, offset, bh, rows, n_keys) >= threshold(p)
+    return draws8(seed, offset, bh, rows, n_keys) >= threshold(p)

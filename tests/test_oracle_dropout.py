@@ -44,15 +44,15 @@ def test_philox_batched_equals_single_calls():
 
 
 def _draw_scalar(seed, offset, bh, i, j):
-    """One entry's 16-bit draw, spelled out from the counter reading."""
-    word = DR.philox4x32_10(np.array([j // 8, i, bh, offset]), (seed % 2**32, seed // 2**32))[(j // 2) % 4]
-    return (int(word) >> (16 * (j % 2))) & 0xFFFF
+    """One entry's 8-bit draw, spelled out from the counter reading."""
+    word = DR.philox4x32_10(np.array([j // 16, i, bh, offset]), (seed % 2**32, seed // 2**32))[(j // 4) % 4]
+    return (int(word) >> (8 * (j % 4))) & 0xFF
 
 
-@pytest.mark.parametrize("Nq,Nk,bh,offset", [(5, 19, 3, 7), (3, 8, 0, 0), (2, 33, 17, 2**32 - 1)])
+@pytest.mark.parametrize("Nq,Nk,bh,offset", [(5, 19, 3, 7), (3, 16, 0, 0), (2, 49, 17, 2**32 - 1)])
 def test_draws_match_per_entry_definition(Nq, Nk, bh, offset):
     seed = 0x0123456789ABCDEF
-    got = DR.draws16(seed, offset, bh, np.arange(Nq), Nk)
+    got = DR.draws8(seed, offset, bh, np.arange(Nq), Nk)
     for i in range(Nq):
         for j in range(Nk):
             assert got[i, j] == _draw_scalar(seed, offset, bh, i, j), (i, j)
@@ -66,10 +66,10 @@ def test_rows_argument_selects_rows():
 
 @pytest.mark.parametrize("p", [0.1, 0.5, 0.9])
 def test_keep_fraction_is_binomial(p):
-    """Over 2^20 entries the kept fraction is within 6 sigma of 1 - t/65536,
+    """Over 2^20 entries the kept fraction is within 6 sigma of 1 - t/256,
     and different heads, offsets and seeds give different masks."""
     m = DR.keep_mask(42, 3, p, 1, 1024, 1024)
-    q = 1.0 - DR.threshold(p) / 65536.0
+    q = 1.0 - DR.threshold(p) / 256.0
     n = m.size
     assert abs(m.mean() - q) < 6 * np.sqrt(q * (1 - q) / n)
     for other in (DR.keep_mask(42, 3, p, 2, 1024, 1024), DR.keep_mask(42, 4, p, 1, 1024, 1024),
@@ -78,11 +78,16 @@ def test_keep_fraction_is_binomial(p):
         assert abs(agree - (q * q + (1 - q) * (1 - q))) < 0.01
 
 
-def test_draws_are_uniform_16_bit():
-    """Chi-square over 256 buckets of the 16-bit draws (2^20 draws)."""
-    d = DR.draws16(7, 0, 0, np.arange(1024), 1024).ravel()
-    assert d.max() < 65536
-    counts = np.bincount(d >> 8, minlength=256)
+def test_draws_are_uniform_8_bit():
+    """Chi-square over the 256 values of the 8-bit draws (2^20 draws), and
+    over the 16 byte positions of a generator call."""
+    d = DR.draws8(7, 0, 0, np.arange(1024), 1024)
+    assert d.max() < 256
+    for pos in range(16):  # each byte of the four output words on its own
+        col = d[:, pos::16].ravel()
+        assert abs(col.mean() - 127.5) < 6 * np.sqrt((256**2 - 1) / 12 / col.size)
+    d = d.ravel()
+    counts = np.bincount(d, minlength=256)
     e = d.size / 256
     chi2 = ((counts - e) ** 2 / e).sum()
     assert chi2 < 255 + 6 * np.sqrt(2 * 255)
@@ -90,9 +95,10 @@ def test_draws_are_uniform_16_bit():
 
 def test_threshold_and_scale():
     assert DR.threshold(0.0) == 0 and DR.keep_scale(0.0) == 1.0
-    assert DR.threshold(0.5) == 32768 and DR.keep_scale(0.5) == 2.0
-    assert DR.threshold(0.1) == 6554
-    for bad in (-0.1, 1.0, 1.0 - 2**-18):
+    assert DR.threshold(0.5) == 128 and DR.keep_scale(0.5) == 2.0
+    assert DR.threshold(0.1) == 26 and DR.keep_scale(0.1) == 256.0 / 230.0
+    assert DR.threshold(0.25) == 64 and DR.keep_scale(0.25) == 256.0 / 192.0
+    for bad in (-0.1, 1.0, 1.0 - 2**-10):
         with pytest.raises(ValueError):
             DR.threshold(bad)
 
