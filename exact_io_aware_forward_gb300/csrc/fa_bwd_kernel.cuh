@@ -91,6 +91,12 @@ struct BwdCfg {
   static constexpr int PT_TILE = (BQ / 64) * PT_SLAB;
   static constexpr int PS = 1;                      // P^T / dS^T buffers
   static constexpr int QS = D == 128 ? 4 : D == 64 ? 3 : 1;  // Q / dO stages
+  // One stage (D = 256): its slabs outside this CTA's feature half are only
+  // read by S^T and dP^T, so they are released and reloaded with the next
+  // tile as soon as those products are done (barriers qo_full / qo_empty),
+  // while the CTA's own half waits for dK / dV.
+  static constexpr bool SPLIT = QS == 1;
+  static_assert(!SPLIT || NP == 2, "the split stage pairs two feature halves");
   // d >= 128: P^T and dS^T also go to TMEM (A operands of dV and dK read from
   // TMEM, saving shared-memory bandwidth); dQ then has one TMEM buffer.
   static constexpr bool PT_TMEM = D != 64;
@@ -106,8 +112,9 @@ struct BwdCfg {
   static constexpr int OFF_KEEP = OFF_LD + 2 * 2 * BQ * 4;
   static constexpr int OFF_BAR = OFF_KEEP + 2 * 2 * BKV * 8;
   // kv_full, q_full[QS], q_empty[QS], sdp_full, sdp_empty, pds_full[PS], pds_empty[PS],
-  // dq_full[2], dq_empty[2], ld_full[2], dkdv_full, drain[3]
-  static constexpr int NBAR = 1 + 2 * QS + 1 + 1 + 2 * PS + 2 + 2 + 2 + 1 + 3 + 8;
+  // dq_full[2], dq_empty[2], ld_full[2], dkdv_full, drain[3], keep_full[4], keep_empty[4],
+  // qo_full, qo_empty
+  static constexpr int NBAR = 1 + 2 * QS + 1 + 1 + 2 * PS + 2 + 2 + 2 + 1 + 3 + 8 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 640;
@@ -212,6 +219,8 @@ __global__ void __launch_bounds__(640, 1)
   uint64_t* keep_full = drain + 3;       // [buffer * 2 + warpgroup]
   uint64_t* keep_empty = keep_full + 4;  // [buffer * 2 + warpgroup]
   uint2* sKeep = reinterpret_cast<uint2*>(smem + C::OFF_KEEP);  // [buffer * 2 + warpgroup][key]
+  uint64_t* qo_full = keep_empty + 4;   // SPLIT: the other feature half of the Q / dO stage
+  uint64_t* qo_empty = qo_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -264,6 +273,8 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(&q_full[b], 1);
       mbar_init(&q_empty[b], 1);
     }
+    mbar_init(qo_full, 1);
+    mbar_init(qo_empty, 2);  // the S^T and dP^T issuers
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dq_full[b], 1);
       mbar_init(&dq_empty[b], 8);
@@ -308,14 +319,27 @@ __global__ void __launch_bounds__(640, 1)
         tma_load_3d(sK + s * C::KV_SLAB, &tm_k, kv_full, s * 64, ck.x, ck.y);
         tma_load_3d(sV + s * C::KV_SLAB, &tm_v, kv_full, s * 64, ck.x, ck.y);
       }
-      int issued = 0;
+      int issued = 0, issued_o = 0;
       for (int it = 0, i = next_tile(i_begin); it < n_it; ++it, i = next_tile(i + 1)) {
         const int b = it % C::QS;
         const uint32_t use = (uint32_t)(it / C::QS);
-        if (!mbar_wait(&q_empty[b], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
-        mbar_arrive_expect_tx(&q_full[b], 2 * C::Q_TILE);
         const int2 cq = sv.qcoord(i * BQ);
+        if constexpr (C::SPLIT) {
+          // the slabs outside this CTA's feature half, once S^T / dP^T of the
+          // previous tile are done with them
+          if (!mbar_wait(qo_empty, (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
+          mbar_arrive_expect_tx(qo_full, 2 * (C::SLABS - C::DA / 64) * C::Q_SLAB);
+          for (int s = 0; s < C::SLABS; ++s) {
+            if (s / (C::DA / 64) == pass) continue;
+            tma_load_3d(sQ + s * C::Q_SLAB, &tm_q, qo_full, s * 64, cq.x, cq.y);
+            tma_load_3d(sDO + s * C::Q_SLAB, &tm_do, qo_full, s * 64, cq.x, cq.y);
+          }
+          issued_o = it + 1;
+        }
+        if (!mbar_wait(&q_empty[b], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
+        mbar_arrive_expect_tx(&q_full[b], C::SPLIT ? 2 * (C::DA / 64) * C::Q_SLAB : 2 * C::Q_TILE);
         for (int s = 0; s < C::SLABS; ++s) {
+          if (C::SPLIT && s / (C::DA / 64) != pass) continue;
           tma_load_3d(sQ + b * C::Q_TILE + s * C::Q_SLAB, &tm_q, &q_full[b], s * 64, cq.x, cq.y);
           tma_load_3d(sDO + b * C::Q_TILE + s * C::Q_SLAB, &tm_do, &q_full[b], s * 64, cq.x, cq.y);
         }
@@ -325,6 +349,7 @@ __global__ void __launch_bounds__(640, 1)
         drain_wait(kv_full, 0);
         for (int it = issued - C::QS < 0 ? 0 : issued - C::QS; it < issued; ++it)
           drain_wait(&q_full[it % C::QS], (uint32_t)((it / C::QS) & 1));
+        if (C::SPLIT && issued_o > 0) drain_wait(qo_full, (uint32_t)((issued_o - 1) & 1));
       }
     }
   } else if (warp >= 1 && warp <= 3) {
@@ -342,6 +367,24 @@ __global__ void __launch_bounds__(640, 1)
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
       const uint32_t aP = smem_u32(sP), aDS = smem_u32(sDS);
       // S^T = K Q^T (warp 1) or dP^T = V dO^T (warp 2) for the tile in stage qs.
+      // SPLIT: the K steps over the other feature half (its slabs arrive
+      // first; the first of them starts the accumulator), then those over
+      // this CTA's half.
+      constexpr int kHalfSteps = C::DA / 16;
+      const int kk_other = pass == 0 ? kHalfSteps : 0;
+      const int kk_own = pass == 0 ? 0 : kHalfSteps;
+      auto issue_sdp_half = [&](int kk0, bool start) {
+        const uint64_t da = sdesc_sw128(warp == 1 ? aK : aV, 16, 1024);
+        const uint64_t db = sdesc_sw128(warp == 1 ? aQ : aDO, 16, 1024);
+        const uint32_t dcol = tmem + (warp == 1 ? C::COL_S : C::COL_DP);
+#pragma unroll
+        for (int t = 0; t < kHalfSteps; ++t) {
+          const int kk = kk0 + t;
+          const uint32_t ok = ((kk >> 2) * C::KV_SLAB + (kk & 3) * 32) >> 4;
+          const uint32_t oq = ((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
+          mma_ss(dcol, da + ok, db + oq, kIdSdP, !(start && t == 0));
+        }
+      };
       auto issue_sdp = [&](int qs) {
         const uint64_t da = sdesc_sw128(warp == 1 ? aK : aV, 16, 1024);
         const uint64_t db = sdesc_sw128((warp == 1 ? aQ : aDO) + qs * C::Q_TILE, 16, 1024);
@@ -391,13 +434,33 @@ __global__ void __launch_bounds__(640, 1)
             mma_ss(tmem + C::COL_DQ + 64 * b, ds0 + o, dk0 + o, kIdDq, kk > 0);
         }
       };
+      // SPLIT: S^T / dP^T of tile t over the other feature half (then that
+      // half of the stage is released), and over this CTA's half.
+      auto sdp_other = [&](int t) {
+        if (!mbar_wait(qo_full, t & 1, abort_flag, status, kStatusTimeout)) return false;
+        tc_fence_after();
+        issue_sdp_half(kk_other, true);
+        mma_commit(qo_empty);
+        return true;
+      };
+      auto sdp_own = [&](int t) {
+        if (!mbar_wait(&q_full[0], t & 1, abort_flag, status, kStatusTimeout)) return false;
+        tc_fence_after();
+        issue_sdp_half(kk_own, false);
+        mma_commit(sdp_full);
+        return true;
+      };
       bool ok = mbar_wait(kv_full, 0, abort_flag, status, kStatusTimeout);
       if (warp <= 2 && n_it > 0) {
-        if (ok) ok = mbar_wait(&q_full[0], 0, abort_flag, status, kStatusTimeout);
-        if (ok) {
-          tc_fence_after();
-          issue_sdp(0);
-          mma_commit(sdp_full);
+        if constexpr (C::SPLIT) {
+          ok = ok && sdp_other(0) && sdp_own(0);
+        } else {
+          if (ok) ok = mbar_wait(&q_full[0], 0, abort_flag, status, kStatusTimeout);
+          if (ok) {
+            tc_fence_after();
+            issue_sdp(0);
+            mma_commit(sdp_full);
+          }
         }
       }
       for (int it = 0; ok && it < n_it; ++it) {
@@ -407,10 +470,16 @@ __global__ void __launch_bounds__(640, 1)
         if (warp <= 2 && it + 1 < n_it) {
           const int qn = (it + 1) % C::QS;
           if (!(ok = mbar_wait(sdp_empty, it & 1, abort_flag, status, kStatusTimeout))) break;
-          if (!(ok = mbar_wait(&q_full[qn], ((it + 1) / C::QS) & 1, abort_flag, status, kStatusTimeout))) break;
-          tc_fence_after();
-          issue_sdp(qn);
-          mma_commit(sdp_full);
+          if constexpr (C::SPLIT) {
+            // warp 1 issues its own half after the dQ product of tile it
+            if (!(ok = sdp_other(it + 1))) break;
+            if (warp == 2 && !(ok = sdp_own(it + 1))) break;
+          } else {
+            if (!(ok = mbar_wait(&q_full[qn], ((it + 1) / C::QS) & 1, abort_flag, status, kStatusTimeout))) break;
+            tc_fence_after();
+            issue_sdp(qn);
+            mma_commit(sdp_full);
+          }
         }
         if (warp == 2) continue;
         if (!(ok = mbar_wait(&pds_full[pb], (it / C::PS) & 1, abort_flag, status, kStatusTimeout))) break;
@@ -420,6 +489,9 @@ __global__ void __launch_bounds__(640, 1)
           issue_dq(pb, b);
           mma_commit(&dq_full[b]);
           mma_commit(&pds_empty[pb]);
+          if constexpr (C::SPLIT) {
+            if (it + 1 < n_it && !(ok = sdp_own(it + 1))) break;
+          }
         } else {
           tc_fence_after();
           issue_dkdv(qs, pb, it == 0);
