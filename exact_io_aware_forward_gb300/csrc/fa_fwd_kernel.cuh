@@ -76,7 +76,7 @@ struct FwdCfg {
   static constexpr int SLAB = 128 * 64 * 2;  // 128 rows x 64 columns x 16 bit
   static constexpr int SLABS = D / 64;
   static constexpr int TILE = SLABS * SLAB;  // one 128 x D tile
-  static constexpr int NS = D == 128 ? 5 : 8;  // K/V ring slots
+  static constexpr int NS = D == 128 ? 4 : 8;  // K/V ring slots (5 at d = 128 measured 0.8% slower)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = QT * TILE;
   static constexpr int OFF_BAR = OFF_RING + NS * TILE;
