@@ -33,7 +33,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one dK/dV launch on C4, from an ncu capture of the current
 # kernel (dram__bytes_read.sum + dram__bytes_write.sum).  Reset to None whenever that kernel
 # changes, until a new capture is taken.
-DKDV_TRAFFIC_C4 = 822376192 + 502333696
+DKDV_TRAFFIC_C4 = 832225024 + 510829568
 
 
 def load_peaks():

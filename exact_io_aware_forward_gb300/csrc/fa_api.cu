@@ -177,7 +177,7 @@ fa_status run_forward(const Shape& s, const void* q, const void* k, const void* 
   const int kv_rows = s.d == 256 ? 64 : 128;  // the d = 256 kernel streams 64-key tiles
   fa::FwdArgs a;
   if (!make_map(&a.tm_q, q, s, false, 128) || !make_map(&a.tm_k, k, s, true, kv_rows) ||
-      !make_map(&a.tm_v, v, s, true, kv_rows))
+      !make_map(&a.tm_v, v, s, true, kv_rows) || !make_map(&a.tm_o, o, s, false, 128))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;
@@ -220,7 +220,8 @@ fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, 
   const int bq = fa::backward_q_tile(s.width());
   fa::BwdArgs a;
   if (!make_map(&a.tm_q, q, s, false, bq) || !make_map(&a.tm_do, dO, s, false, bq) ||
-      !make_map(&a.tm_k, k, s, true, 128) || !make_map(&a.tm_v, v, s, true, 128))
+      !make_map(&a.tm_k, k, s, true, 128) || !make_map(&a.tm_v, v, s, true, 128) ||
+      !make_map(&a.tm_dk, dk, s, true, 128) || !make_map(&a.tm_dv, dv, s, true, 128))
     return FA_ERR_CUDA;
   a.dk = dk;
   a.dv = dv;

@@ -183,10 +183,50 @@ __device__ __forceinline__ void store_rows_from_tmem(uint32_t taddr, uint4* dst,
   }
 }
 
+// The same rows (all 128, times `mul`) into the 128-byte-swizzled shared-memory
+// slabs of a TMA store, 64 columns (128 rows x 128 bytes) per slab; `zero`
+// stages zeros instead.
+template <int DA, bool BF16>
+__device__ __forceinline__ void stage_rows_from_tmem(uint32_t taddr, uint8_t* stage, int r, float mul, bool zero) {
+#pragma unroll
+  for (int c = 0; c < DA / 32; ++c) {
+    uint32_t pk[16];
+    if (zero) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] = 0u;
+    } else {
+      float v[32];
+      tmem_ld32(taddr + 32 * c, v);
+      tmem_ld_wait(v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] = pack2(v[2 * i] * mul, v[2 * i + 1] * mul, BF16);
+    }
+    uint8_t* slab = stage + ((32 * c) >> 6) * (128 * 128);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(slab + sw128_offset(r, (32 * c & 63) + 8 * q)) =
+          make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  }
+}
+
+// One thread of a warpgroup stores the staged 128 x DA tile (rows from key
+// kv0 of head `bh`, features from feat0) with TMA; rows past Nk and features
+// past dh fall outside the tensor map and are not written.
+template <int DA>
+__device__ __forceinline__ void store_staged_tile(const CUtensorMap* m, const uint8_t* stage, int feat0, int dh,
+                                                  int2 coord) {
+#pragma unroll
+  for (int sl = 0; sl < DA / 64; ++sl)
+    if (feat0 + 64 * sl < dh) tma_store_3d(m, stage + sl * (128 * 128), feat0 + 64 * sl, coord.x, coord.y);
+  tma_store_commit();
+  tma_store_wait_read();
+}
+
 template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(640, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                        void* __restrict__ dk, void* __restrict__ dv, const float* __restrict__ lse,
                        const float* __restrict__ delta, float* __restrict__ dq_accum, SeqLayout lay, int BH,
                        float scale, float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads,
@@ -645,14 +685,23 @@ __global__ void __launch_bounds__(640, 1)
     }
     if (h == 0) {
       if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
-      if (ok) {
-        tc_fence_after();
+      if (ok) tc_fence_after();
+      // n_it == 0: no query sees this key tile (block mask, or causal with Nq < Nk): dV = 0
+      if constexpr (!VARLEN) {
+        // Dense rows: stage the tile in the (now unused) Q stages, store with
+        // TMA; every warp of the warpgroup reaches the barrier once.
+        if (ok) stage_rows_from_tmem<C::DA, BF16>(lane_base + C::COL_DV, sQ, r, DROP ? drop.keep_scale : 1.f,
+                                                  n_it == 0);
+        fence_async_smem();
+        named_barrier_sync(1, 128);
+        if (r == 0 && ok && !*abort_flag) store_staged_tile<C::DA>(&tm_dv, sQ, feat0, dh, sv.kcoord(kv0));
+      } else if (ok) {
         uint4* dst = reinterpret_cast<uint4*>(dv) + sv.kflat(key) * (dh / 8) + feat0 / 8;
         const int cols = min(C::DA, dh - feat0);  // features of this CTA that exist
         if (n_it > 0) {
           store_rows_from_tmem<C::DA, BF16>(lane_base + C::COL_DV, dst, key < Nk, DROP ? drop.keep_scale : 1.f,
                                             cols);
-        } else if (key < Nk) {  // no query sees this key tile (block mask, or causal with Nq < Nk): dV = 0
+        } else if (key < Nk) {
           for (int q = 0; q < cols / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
@@ -711,8 +760,13 @@ __global__ void __launch_bounds__(640, 1)
     }
     if (g == 0) {
       if (ok) ok = warp_wait(dkdv_full, 0, abort_flag, status);
-      if (ok) {
-        tc_fence_after();
+      if (ok) tc_fence_after();
+      if constexpr (!VARLEN) {  // as dV, staged in the dO stages
+        if (ok) stage_rows_from_tmem<C::DA, BF16>(lane_base + C::COL_DK, sDO, r, scale, n_it == 0);
+        fence_async_smem();
+        named_barrier_sync(2, 128);
+        if (r == 0 && ok && !*abort_flag) store_staged_tile<C::DA>(&tm_dk, sDO, feat0, dh, sv.kcoord(kv0));
+      } else if (ok) {
         const int key = kv0 + r;
         uint4* dst = reinterpret_cast<uint4*>(dk) + sv.kflat(key) * (dh / 8) + feat0 / 8;
         const int cols = min(C::DA, dh - feat0);
@@ -752,7 +806,8 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t stream) {
   const int n_kv = (a.lay.Nk + C::BKV - 1) / C::BKV;
   const long long grid = (long long)n_kv * a.BH * C::NP;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dk, a.dv, a.lse,
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.tm_dk, a.tm_dv, a.dk,
+                                                         a.dv, a.lse,
                                                          a.delta, a.dq_accum, a.lay, a.BH, a.scale, a.scale_log2,
                                                          a.block_mask, a.mask_heads, a.drop, heads_per_group(a, D),
                                                          a.status);

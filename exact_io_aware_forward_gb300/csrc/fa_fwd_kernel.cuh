@@ -132,7 +132,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  void* __restrict__ o,
                   float* __restrict__ lse, SeqLayout lay, int BH, int n_qblocks, float scale_log2,
                   const uint8_t* __restrict__ block_mask, int mask_heads, DropParams drop, int group,
                   unsigned int* status) {
@@ -527,15 +528,21 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     // ------------------------------------------------------------ epilogue
+    // Block-sparse and dropout instances (dense layouts) stage O in shared
+    // memory and store it with TMA; the plain dense instances measured
+    // faster with per-row stores, and packed layouts need them (a tile's
+    // last rows can belong to the next sequence).
+    constexpr bool kStageO = !VARLEN && (SPARSE || DROP);
     if (ok) ok = warp_wait(o_full, 0, abort_flag, status);
     const long long frow = sv.qflat(row);
+    const bool has_o = ok && c > 0;
     if (ok && c == 0) {  // no key tile for this query tile: empty softmax, O = 0, LSE = -inf
       uint4* orow = reinterpret_cast<uint4*>(o) + frow * (dh / 8);
       if (row < Nq) {
         for (int q = 0; q < dh / 8; ++q) orow[q] = make_uint4(0u, 0u, 0u, 0u);
         lse[frow] = neg_inf();
       }
-    } else if (ok) {
+    } else if (has_o) {
       tc_fence_after();
       // O is divided by the sum of the rounded weights that entered the MMA,
       // so each output row stays a convex combination of V rows; the
@@ -544,25 +551,62 @@ __global__ void __launch_bounds__(384, 1)
       // A row that saw no key (bottom-right causal with Nq > Nk) has l = 0 and
       // O = 0 in TMEM: it stays 0, and its LSE is -inf.
       const float inv_l = l_mma > 0.f ? (DROP ? drop.keep_scale : 1.f) / l_mma : 0.f;
-      // Each thread writes its own row: dh/8 16-byte chunks, contiguous in memory.
-      uint4* orow = reinterpret_cast<uint4*>(o) + frow * (dh / 8);
+      if constexpr (kStageO) {
+        // The warpgroup stages its 128 x D tile of O in the (now unused)
+        // shared-memory tile of Q_t, in the 128-byte-swizzled slabs the O
+        // tensor map describes; one thread stores it with TMA below.
+        uint8_t* stage = sQ + t * C::TILE;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        if (32 * cc >= dh) break;  // features past dh (zero-padded inputs) are not stored
-        float ov[32];
-        tmem_ld32(tO + 32 * cc, ov);
-        tmem_ld_wait(ov);
-        uint32_t pk[16];
+        for (int cc = 0; cc < D / 32; ++cc) {
+          float ov[32];
+          tmem_ld32(tO + 32 * cc, ov);
+          tmem_ld_wait(ov);
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, BF16);
-        if (row < Nq) {
+          for (int i = 0; i < 16; ++i) pk[i] = pack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, BF16);
+          uint8_t* slab = stage + ((32 * cc) >> 6) * C::SLAB;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) orow[4 * cc + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(slab + sw128_offset(r, (32 * cc & 63) + 8 * q)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      } else {
+        // Each thread writes its own row: dh/8 16-byte chunks, contiguous in memory.
+        uint4* orow = reinterpret_cast<uint4*>(o) + frow * (dh / 8);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          if (32 * cc >= dh) break;  // features past dh (zero-padded inputs) are not stored
+          float ov[32];
+          tmem_ld32(tO + 32 * cc, ov);
+          tmem_ld_wait(ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, BF16);
+          if (row < Nq) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) orow[4 * cc + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
         }
       }
       if (row < Nq) {
         const float m_fin = (m_ref == neg_inf()) ? 0.f : m_ref;
         lse[frow] = (m_fin + __log2f(l)) * kLn2;
+      }
+    }
+    if constexpr (kStageO) {
+      // Every warp of the warpgroup reaches this barrier once, whatever its
+      // path above; rows past Nq and features past dh fall outside the O map
+      // and are not written.
+      fence_async_smem();
+      named_barrier_sync(1 + t, 128);
+      const int row0 = q0 + t * C::BM;
+      if (r == 0 && has_o && row0 < Nq && !*abort_flag) {
+        const int2 cq = sv.qcoord(row0);
+#pragma unroll
+        for (int sl = 0; sl < C::SLABS; ++sl)
+          if (64 * sl < dh) tma_store_3d(&tm_o, sQ + t * C::TILE + sl * C::SLAB, 64 * sl, cq.x, cq.y);
+        tma_store_commit();
+        tma_store_wait_read();
       }
     }
   }
@@ -587,7 +631,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   // K and V of a head take 4 * Nk * D bytes; a group keeps them within ~64 MB of L2.
   const long long per_head = 4LL * a.lay.Nk * D;
   const int group = (int)std::max(1LL, std::min(64LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.lay, a.BH, n_qblocks,
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.o, a.lse, a.lay, a.BH,
+                                                         n_qblocks,
                                                          a.scale_log2, a.block_mask, a.mask_heads, a.drop, group,
                                                          a.status);
   return cudaGetLastError();

@@ -56,6 +56,7 @@ struct DropParams {
 
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;        // 3-D maps, box 64 columns x 128 rows (see make_map)
+  CUtensorMap tm_o;                    // O, box 64 columns x 128 rows (TMA-stored epilogues)
   void* o;                             // layout `lay`
   float* lse;
   SeqLayout lay;
@@ -78,6 +79,7 @@ cudaError_t launch_forward256(bool causal, bool bf16, const FwdArgs& a, cudaStre
 struct BwdArgs {
   CUtensorMap tm_q, tm_do;         // box 64 columns x BQ rows
   CUtensorMap tm_k, tm_v;          // box 64 columns x 128 rows
+  CUtensorMap tm_dk, tm_dv;        // box 64 columns x 128 rows (dense layouts: epilogue stores)
   void* dk;                        // layout `lay` (key side)
   void* dv;
   const float* lse;                // one float per query row
