@@ -311,9 +311,9 @@ fa_status fa_device_status(void* stream);
 
 /*
  * Work counters, for checking which score tiles the kernels compute.  The
- * tiled algorithm (Tri Dao's FlashAttention notes, section 04.5 "Causal
- * Masking": a tile lying wholly above the diagonal is skipped) visits
- * T(T+1)/2 of the T x T square tiles under the causal mask, and the
+ * tiled algorithm ("FlashAttention 为什么不需要存下注意力矩阵", jefxiong.cn,
+ * section 04.5: a tile lying wholly above the causal diagonal is skipped)
+ * visits T(T+1)/2 of the T x T square tiles under the causal mask, and the
  * block-sparse variant only the kept blocks.  Every forward and dK/dV kernel
  * adds the score blocks it computed, in units of 64 query rows x 64 keys
  * (a 128 x 128 tile counts 4), to one of two 64-bit device counters: the

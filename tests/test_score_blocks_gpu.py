@@ -1,9 +1,9 @@
 """Work counters: the score tiles the kernels compute (whole-tile causal skip,
 block-sparse skip) against closed forms.
 
-Tri Dao's FlashAttention notes, section 04.5 ("Causal Masking"): a tile that
-lies wholly above the diagonal is skipped, so T(T+1)/2 of the T x T square
-tiles are visited (2080 of 4096 at 64-row blocks and N = 4096; at the
+"FlashAttention 为什么不需要存下注意力矩阵" (jefxiong.cn), section 04.5: a tile
+that lies wholly above the causal diagonal is skipped, so T(T+1)/2 of the T x T
+square tiles are visited (2080 of 4096 at 64-row blocks and N = 4096; at the
 kernels' 128-row tiles the same rule gives 528 of 1024).  The counters count
 64 x 64 score blocks, so a 128 x 128 tile is 4 of them.
 
