@@ -754,6 +754,7 @@ def run_gpu(args, w, world, rank, local):
         from exact_io_aware_forward_gb300.synth import S1
         from exact_io_aware_forward_gb300.synth import V1
         from exact_io_aware_forward_gb300.synth import W96, W256
+        result["long"] = measure_long(dev, peak)
         for key, kind, vw in (("blocksparse", "blocksparse", S1), ("dropout", "dropout", w), ("varlen", "varlen", V1),
                               ("d96", "dense", W96), ("d256", "dense", W256)):
             sms, sparts, _, sbufs = measure_variant(dev, kind, vw, 10, 3)
@@ -765,6 +766,33 @@ def run_gpu(args, w, world, rank, local):
     if dist:
         dist.destroy_process_group()
     return result
+
+
+def measure_long(dev, peak):
+    """The long-sequence workload (C5: causal, B=1, H=8, N=32768, d=128): fwd,
+    dK/dV and fwd+bwd throughput, and the peak device memory of its fwd+bwd
+    steps (inputs, outputs and the O(N) workspace) against the 2*N^2*2 bytes
+    per head that a naive path would spend on S and P."""
+    import torch
+
+    from exact_io_aware_forward_gb300.synth import C5 as w
+    torch.cuda.synchronize(dev)
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    ms, parts, _, bufs = measure_variant(dev, "dense", w, 10, 3)
+    torch.cuda.synchronize(dev)
+    used = torch.cuda.max_memory_allocated(dev) - base
+    F = w.fwd_flops()
+    elem = w.B * w.H * w.N * w.d * 2
+    return {"workload": w.name, "ms": round(ms, 4), "fwdbwd_tflops": round(2.5 * F / (ms * 1e-3) / 1e12, 1),
+            "fwdbwd_frac_of_peak": round(2.5 * F / (ms * 1e-3) / 1e12 / peak, 4),
+            "fwd_tflops": round(F / (parts[0] * 1e-3) / 1e12, 1),
+            "fwd_frac_of_peak": round(F / (parts[0] * 1e-3) / 1e12 / peak, 4),
+            "dkdv_frac_of_peak": round(2.5 * F / (parts[2] * 1e-3) / 1e12 / peak, 4),
+            "peak_memory_bytes": int(used), "inputs_bytes": int(4 * elem),
+            "naive_sp_bytes": int(2 * w.N * w.N * 2 * w.B * w.H),
+            "memory": "peak torch allocation of the fwd+bwd steps above the allocations before them: Q, K, V, dO, "
+                      "O, LSE, dQ, dK, dV and the backward workspace"}
 
 
 def run_reference(args, w, world, rank):

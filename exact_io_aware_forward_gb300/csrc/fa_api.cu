@@ -260,13 +260,27 @@ size_t workspace_bytes_for(const Shape& s) {
   return align256(rows * sizeof(float)) + align256(rows * s.d * sizeof(float));
 }
 
+// Everything run_backward checks except the workspace: scale, head dim with a
+// block mask, and every tensor pointer (non-null, 16-byte aligned).
+fa_status check_backward(const Shape& s, const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, const void* dq, const void* dk, const void* dv, const uint8_t* block_mask,
+                         float scale) {
+  fa_status st = check_scale(scale);
+  if (st != FA_OK) return st;
+  if (s.d == 256 && block_mask) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
 fa_status run_backward(const Shape& s, const void* q, const void* k, const void* v, const void* o, const void* dO,
                        const float* lse, void* dq, void* dk, void* dv, const uint8_t* block_mask, int mask_heads,
                        int causal, float scale, void* workspace, size_t workspace_bytes, void* stream,
                        const fa::DropParams* drop) {
-  fa_status st = check_scale(scale);
+  // Every argument is checked here, before the first of the three launches.
+  fa_status st = check_backward(s, q, k, v, o, dO, lse, dq, dk, dv, block_mask, scale);
   if (st != FA_OK) return st;
-  if (s.d == 256 && block_mask) return FA_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < workspace_bytes_for(s))
     return FA_ERR_WORKSPACE;
   float* delta = static_cast<float*>(workspace);
@@ -280,6 +294,17 @@ fa_status run_backward(const Shape& s, const void* q, const void* k, const void*
 }
 
 }  // namespace
+
+namespace fa {
+int backward_arguments_status(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, const void* dq, const void* dk, const void* dv, int B, int H, int N,
+                              int d, int dtype, float scale) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  return check_backward(s, q, k, v, o, dO, lse, dq, dk, dv, nullptr, scale);
+}
+}  // namespace fa
 
 // ---------------------------------------------------------------- entry points
 extern "C" {

@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "../../include/fa_gb300.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -51,26 +52,21 @@ void* scratch_on_current_device() {
   return g_scratch_ptr[dev];
 }
 
-size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
-
 }  // namespace
 
 extern "C" fa_status fa_backward_noalloc(const void* q, const void* k, const void* v, const void* o,
                                          const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                                          int H, int N, int d, int dtype, int causal, float scale,
                                          void* stream) {
-  const size_t need = fa_backward_workspace_size(B, H, N, d);
-  if (need == 0) return (d == 64 || d == 128) ? FA_ERR_INVALID_ARG : FA_ERR_UNSUPPORTED;
-  if (need > kScratchBytes) return FA_ERR_SCRATCH_TOO_SMALL;
-  char* base = static_cast<char*>(scratch_on_current_device());
+  // Invalid arguments get the status fa_backward gives them, before any CUDA
+  // call; only then does the size of the problem matter.
+  const int st = fa::backward_arguments_status(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, dtype, scale);
+  if (st != FA_OK) return static_cast<fa_status>(st);
+  if (fa_backward_workspace_size(B, H, N, d) > kScratchBytes) return FA_ERR_SCRATCH_TOO_SMALL;
+  void* base = scratch_on_current_device();
   if (base == nullptr) return FA_ERR_CUDA;
-  // Same layout as the fa_backward workspace: D, then the dQ accumulator.
-  const size_t rows = (size_t)B * H * N;
-  float* delta = reinterpret_cast<float*>(base);
-  float* dq_accum = reinterpret_cast<float*>(base + round256(rows * sizeof(float)));
-  fa_status st = fa_backward_preprocess(o, dO, delta, dq_accum, B, H, N, d, dtype, stream);
-  if (st != FA_OK) return st;
-  st = fa_backward_dkdv(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H, N, d, dtype, causal, scale, stream);
-  if (st != FA_OK) return st;
-  return fa_backward_dq_convert(dq_accum, dq, B, H, N, d, dtype, scale, stream);
+  // D and the dQ accumulator are laid out in the scratch exactly as in a
+  // caller's workspace.
+  return fa_backward(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, dtype, causal, scale, base, kScratchBytes,
+                     stream);
 }

@@ -78,7 +78,8 @@ template <bool CAUSAL, bool BF16, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(192, 1)
     fa_fwd256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o, float* __restrict__ lse,
-                     SeqLayout lay, int BH, int n_qblocks, float scale_log2, DropParams drop, unsigned int* status) {
+                     SeqLayout lay, int BH, int n_qblocks, float scale_log2, DropParams drop, int group,
+                     unsigned int* status) {
   using C = Fwd256Cfg;
   constexpr int D = C::D;
   extern __shared__ uint8_t smem_raw[];
@@ -100,9 +101,14 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Heaviest work first: under the causal mask the last query blocks see the most keys.
-  const int bh = blockIdx.x % BH;
-  const int qb = n_qblocks - 1 - blockIdx.x / BH;
+  // Heads in groups of `group` (a group's K and V fit in about half of L2, so
+  // they are read from DRAM about once); inside a group the heaviest work
+  // first: under the causal mask the last query blocks see the most keys.
+  const int gi = blockIdx.x / (group * n_qblocks);
+  const int heads = min(group, BH - gi * group);  // the last group may be smaller
+  const int within = blockIdx.x - gi * group * n_qblocks;
+  const int bh = gi * group + within % heads;
+  const int qb = n_qblocks - 1 - within / heads;
   const int q0 = qb * C::BM;
   const SeqView sv = seq_view<VARLEN>(lay, bh);
   if (!sv.ok && q0 == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSeqlens);
@@ -396,8 +402,11 @@ cudaError_t launch_fwd256_t(const FwdArgs& a, cudaStream_t stream) {
   const int n_qblocks = (a.lay.Nq + C::BM - 1) / C::BM;
   const long long grid = (long long)n_qblocks * a.BH;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // K and V of a head take 4 * Nk * 256 bytes; a group keeps them within ~64 MB of L2.
+  const long long per_head = 4LL * a.lay.Nk * C::D;
+  const int group = (int)std::max(1LL, std::min(64LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.lay, a.BH, n_qblocks,
-                                                         a.scale_log2, a.drop, a.status);
+                                                         a.scale_log2, a.drop, group, a.status);
   return cudaGetLastError();
 }
 

@@ -95,6 +95,11 @@ struct BwdArgs {
   DropParams drop;
   unsigned int* status;
 };
+// The status fa_backward returns for these arguments before it looks at its
+// workspace (FA_OK when shape, dtype, scale and every pointer are valid).
+int backward_arguments_status(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, const void* dq, const void* dk, const void* dv, int B, int H, int N,
+                              int d, int dtype, float scale);
 int backward_q_tile(int d);  // query rows per inner iteration of the dK/dV kernel
 cudaError_t launch_backward_dkdv(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_backward_dkdv_dropout(int d, bool causal, bool bf16, const BwdArgs& a, cudaStream_t stream);

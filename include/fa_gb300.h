@@ -290,7 +290,9 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o
  * The D vector and the fp32 dQ accumulator live in a static device array of
  * FA_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading the library keeps
  * until the process exits.  Problems with fa_backward_workspace_size() larger
- * than that return FA_ERR_SCRATCH_TOO_SMALL before any launch.  The first
+ * than that return FA_ERR_SCRATCH_TOO_SMALL before any launch; any other
+ * invalid argument gets the status fa_backward returns for it, checked
+ * first and before any CUDA call.  The first
  * call on a device looks up the array's address with that device current;
  * make it before any stream capture starts.  All calls share the array:
  * calls that overlap on the GPU race and must be serialised.  Each call

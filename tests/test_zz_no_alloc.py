@@ -33,6 +33,41 @@ def test_rejects_problems_beyond_the_scratch():
     assert "32 MiB" in _lib.status_string(rc)
 
 
+BAD_CALLS = {
+    # name: (argument overrides); every pointer is aligned and never dereferenced
+    "zero_batch_d96": dict(B=0, d=96),
+    "zero_n_d256": dict(N=0, d=256),
+    "beyond_2_31": dict(H=16, N=1 << 20, d=128),
+    "head_dim_80": dict(d=80),
+    "dtype_7": dict(dt=7),
+    "nan_scale": dict(scale=float("nan")),
+    "negative_scale": dict(scale=-0.5),
+    "null_q": dict(q=None),
+    "null_lse": dict(lse=None),
+    "misaligned_dq": dict(dq=(1 << 20) + 4),
+    "misaligned_dv": dict(dv=(1 << 20) + 8),
+}
+
+
+@pytest.mark.parametrize("case", sorted(BAD_CALLS))
+def test_invalid_arguments_get_the_status_of_fa_backward(case):
+    """Both entry points reject the same bad call with the same status, before
+    any launch (the pointers are never dereferenced; no GPU is needed)."""
+    from exact_io_aware_forward_gb300 import build as fa_build
+    fa_build.build()
+    lib = _lib.lib()
+    ptr = 1 << 20
+    a = dict(q=ptr, k=ptr, v=ptr, o=ptr, do=ptr, lse=ptr, dq=ptr, dk=ptr, dv=ptr, B=1, H=2, N=64, d=64, dt=1,
+             causal=1, scale=0.125)
+    a.update(BAD_CALLS[case])
+    tensors = [a[n] for n in ("q", "k", "v", "o", "do", "lse", "dq", "dk", "dv")]
+    rest = [a["B"], a["H"], a["N"], a["d"], a["dt"], a["causal"], a["scale"]]
+    want = lib.fa_backward(*tensors, *rest, ptr, 1 << 30, None)
+    got = lib.fa_backward_noalloc(*tensors, *rest, None)
+    assert want in (1, 2), _lib.status_string(want)
+    assert got == want, (_lib.status_string(got), _lib.status_string(want))
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("B,H,N,d,dtype,causal", [(1, 4, 1000, 128, "bf16", True),
                                                    (2, 3, 515, 64, "fp16", False),
