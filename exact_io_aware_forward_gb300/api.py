@@ -289,10 +289,11 @@ def fa_backward_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal=False, scale=Non
 
 
 def fa_backward_preprocess(o, do, delta, dq_accum, stream=None) -> None:
+    """D = rowsum(dO * O) into ``delta``; ``dq_accum`` zeroed, or None (D only)."""
     B, H, N, d = _shape(o)
     dt = o.dtype
     args = [_bhnd("o", o), _bhnd("do", do, o.shape, dt), _bhnd("delta", delta, (B, H, N), torch.float32),
-            _bhnd("dq_accum", dq_accum, o.shape, torch.float32)]
+            None if dq_accum is None else _bhnd("dq_accum", dq_accum, o.shape, torch.float32)]
     _check("fa_backward_preprocess",
            lib().fa_backward_preprocess(*args, B, H, N, d, _DTYPE_CODE[dt], _stream(stream)))
 
@@ -319,6 +320,28 @@ def fa_backward_dkdv_blocksparse(q, k, v, do, lse, delta, dq_accum, dk, dv, bloc
             _bhnd("dv", dv, q.shape, dt)]
     _check("fa_backward_dkdv_blocksparse", lib().fa_backward_dkdv_blocksparse(
         *args, mptr, mheads, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), _stream(stream)))
+
+
+def fa_backward_dk_dv(q, k, v, do, lse, delta, dk, dv, causal=False, scale=None, stream=None) -> None:
+    """Split backward: dK and dV (no dQ work)."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dk", dk, q.shape, dt), _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_dk_dv", lib().fa_backward_dk_dv(*args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)),
+                                                        _scale(scale, d), _stream(stream)))
+
+
+def fa_backward_dq(q, k, v, do, lse, delta, dq, causal=False, scale=None, stream=None) -> None:
+    """Split backward: dQ by its own kernel (recomputes P and dP)."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dq", dq, q.shape, dt)]
+    _check("fa_backward_dq", lib().fa_backward_dq(*args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)),
+                                                  _scale(scale, d), _stream(stream)))
 
 
 def fa_backward_dq_convert(dq_accum, dq, scale=None, stream=None) -> None:

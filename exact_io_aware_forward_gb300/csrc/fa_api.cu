@@ -199,9 +199,11 @@ fa_status run_forward(const Shape& s, const void* q, const void* k, const void* 
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// dq_accum may be null: then only D is computed (the split backward needs no accumulator).
 fa_status run_preprocess(const Shape& s, const void* o, const void* dO, float* delta, float* dq_accum,
                          void* stream) {
-  if (!aligned16(o) || !aligned16(dO) || !aligned16(delta) || !aligned16(dq_accum)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(delta) || (dq_accum && !aligned16(dq_accum)))
+    return FA_ERR_INVALID_ARG;
   if (fa::launch_backward_preprocess(s.d, s.bf16(), o, dO, delta, dq_accum, s.q_rows(),
                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FA_ERR_CUDA;
@@ -242,6 +244,39 @@ fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, 
   const cudaError_t e = s.varlen()  ? fa::launch_backward_dkdv_varlen(s.width(), causal != 0, s.bf16(), a, cs)
                         : a.dropout ? fa::launch_backward_dkdv_dropout(s.width(), causal != 0, s.bf16(), a, cs)
                                     : fa::launch_backward_dkdv(s.width(), causal != 0, s.bf16(), a, cs);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// The two stages of the split backward: dK and dV (want_dq false) or dQ
+// (want_dq true), each recomputing P and dP; dense layouts, d in {64, 96, 128}.
+fa_status run_split(const Shape& s, bool want_dq, const void* q, const void* k, const void* v, const void* dO,
+                    const float* lse, const float* delta, void* dq, void* dk, void* dv, int causal, float scale,
+                    void* stream) {
+  fa_status st = check_scale(scale);
+  if (st != FA_OK) return st;
+  if (s.varlen() || s.width() == 256) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) || !aligned16(delta))
+    return FA_ERR_INVALID_ARG;
+  if (want_dq ? !aligned16(dq) : (!aligned16(dk) || !aligned16(dv))) return FA_ERR_INVALID_ARG;
+  fa::SplitArgs a;
+  if (!make_map(&a.tm_q, q, s, false, 128) || !make_map(&a.tm_do, dO, s, false, 128) ||
+      !make_map(&a.tm_k, k, s, true, 128) || !make_map(&a.tm_v, v, s, true, 128))
+    return FA_ERR_CUDA;
+  if (!want_dq && (!make_map(&a.tm_dk, dk, s, true, 128) || !make_map(&a.tm_dv, dv, s, true, 128)))
+    return FA_ERR_CUDA;
+  a.dq = dq;
+  a.lse = lse;
+  a.delta = delta;
+  a.N = s.lay.Nq;
+  a.BH = s.B * s.H;
+  a.dh = s.d;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.status = status_word();
+  if (!a.status) return FA_ERR_CUDA;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = want_dq ? fa::launch_backward_dq(s.width(), causal != 0, s.bf16(), a, cs)
+                                : fa::launch_backward_dkdv_split(s.width(), causal != 0, s.bf16(), a, cs);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -286,6 +321,16 @@ fa_status run_backward(const Shape& s, const void* q, const void* k, const void*
   float* delta = static_cast<float*>(workspace);
   float* dq_accum =
       reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)s.q_rows() * sizeof(float)));
+  // Dense attention without a block mask or dropout at d <= 128 takes the
+  // split backward (dQ by its own kernel, no accumulator); the rest
+  // accumulates dQ in the dK / dV kernel.
+  const bool split = !s.varlen() && !block_mask && !(drop && drop->t > 0) && s.width() != 256;
+  if (split) {
+    if ((st = run_preprocess(s, o, dO, delta, nullptr, stream)) != FA_OK) return st;
+    if ((st = run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, causal, scale, stream)) != FA_OK)
+      return st;
+    return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, causal, scale, stream);
+  }
   if ((st = run_preprocess(s, o, dO, delta, dq_accum, stream)) != FA_OK) return st;
   if ((st = run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, causal, scale, stream,
                      drop)) != FA_OK)
@@ -485,6 +530,24 @@ fa_status fa_backward_dkdv_dropout(const void* q, const void* k, const void* v, 
   fa::DropParams dp;
   if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
   return run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, causal, scale, stream, &dp);
+}
+
+fa_status fa_backward_dk_dv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                            const float* delta, void* dk, void* dv, int B, int H, int N, int d, int dtype, int causal,
+                            float scale, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, causal, scale, stream);
+}
+
+fa_status fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                         const float* delta, void* dq, int B, int H, int N, int d, int dtype, int causal, float scale,
+                         void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, causal, scale, stream);
 }
 
 fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,

@@ -1,6 +1,7 @@
 // Memory-bound helper kernels of the backward pass.
 //
-//   preprocess:  D_i = sum_c dO_ic * O_ic (float32) and dq_accum := 0.
+//   preprocess:  D_i = sum_c dO_ic * O_ic (float32) and, when an accumulator
+//                is given, dq_accum := 0.
 //                D replaces rowsum(P * (dO V^T)) of the softmax backward
 //                ("FlashAttention 为什么不需要存下注意力矩阵", jefxiong.cn,
 //                section 3.3): sum_j P_ij (dO_i . V_j) = dO_i . (P V)_i = dO_i . O_i.
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const uint4* __r
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
     if (active) {
       if (part == 0) delta[row] = acc;
+      if (dq_accum == nullptr) continue;  // D only (the split backward keeps no accumulator)
 #pragma unroll
       for (int u = 0; u < VPT; ++u) {
         dq_accum[2 * (idx0 + u)] = zero;

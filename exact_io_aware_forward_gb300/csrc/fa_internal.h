@@ -107,6 +107,22 @@ cudaError_t launch_backward_dkdv_varlen(int d, bool causal, bool bf16, const Bwd
 // keep[bh][i][j] = 1 if entry (bh, i, j) is kept, else 0 ([BH, Nq, Nk] bytes).
 cudaError_t launch_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, const DropParams& drop,
                                      cudaStream_t stream);
+// The backward pass with dQ computed by a kernel of its own (dense layouts,
+// no block mask, no dropout): a dK / dV kernel and a dQ kernel that both
+// recompute P and dP on chip.
+struct SplitArgs {
+  CUtensorMap tm_q, tm_do;         // box 64 columns x 128 rows
+  CUtensorMap tm_k, tm_v;          // box 64 columns x 128 rows
+  CUtensorMap tm_dk, tm_dv;        // box 64 columns x 128 rows (epilogue stores)
+  void* dq;                        // [B, H, N, dh] 16-bit
+  const float* lse;
+  const float* delta;
+  int N, BH, dh;
+  float scale, scale_log2;
+  unsigned int* status;
+};
+cudaError_t launch_backward_dkdv_split(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream);
+cudaError_t launch_backward_dq(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream);
 cudaError_t launch_backward_preprocess(int d, bool bf16, const void* o, const void* dO, float* delta,
                                        float* dq_accum, long long rows, cudaStream_t stream);
 cudaError_t launch_backward_dq_convert(int d, bool bf16, const float* dq_accum, void* dq, long long rows,

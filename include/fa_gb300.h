@@ -107,8 +107,14 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  * tile as exp(s * Q K^T - LSE),
  *   dS = P * (G V^T - D),  D_i = sum_c dO_ic O_ic  ( = rowsum(P * (G V^T)) ),
  *   dQ = s dS K,  dK = s dS^T Q,  dV = P^T G.
- * Runs fa_backward_preprocess, fa_backward_dkdv and fa_backward_dq_convert
- * in that order on `stream`.  `workspace` must hold
+ * Two strategies for dQ, both exact (chosen per call, see below):
+ *   - split (dense attention, d in {64, 96, 128}): fa_backward_preprocess
+ *     with dq_accum = NULL, fa_backward_dk_dv, fa_backward_dq -- dQ by a
+ *     kernel of its own that recomputes P and dP, no float32 accumulator;
+ *   - accumulated (d = 256): fa_backward_preprocess, fa_backward_dkdv,
+ *     fa_backward_dq_convert -- dQ partials added into a float32
+ *     accumulator by the dK / dV kernel.
+ * All stages run in order on `stream`.  `workspace` must hold
  * fa_backward_workspace_size(B,H,N,d) bytes (else FA_ERR_WORKSPACE); its
  * contents on entry do not matter and are overwritten.
  * o and lse are the forward outputs for the same q, k, v, causal and scale.
@@ -181,7 +187,8 @@ fa_status fa_selftest_wait_timeout(void* stream);
  * Stage 1 of the backward pass: D_i = sum_c dO_ic * O_ic in float32 (the
  * row-sum shortcut for rowsum(P * (dO V^T)), which holds because O = P V),
  * and dq_accum := 0.  delta: [B,H,N] float32 out; dq_accum: [B,H,N,d]
- * float32 out.
+ * float32 out, or NULL (only D is computed; the split backward needs no
+ * accumulator).
  */
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* delta, float* dq_accum, int B, int H,
                                  int N, int d, int dtype, void* stream);
@@ -211,6 +218,31 @@ fa_status fa_backward_dkdv_blocksparse(const void* q, const void* k, const void*
 /* Stage 3: dq = scale * dq_accum, rounded to dtype. */
 fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,
                                  float scale, void* stream);
+
+/*
+ * The split backward (tutorial section 3.3 with the dQ sum done apart from
+ * dK and dV), after fa_backward_preprocess(o, dO, delta, NULL, ...):
+ *
+ * fa_backward_dk_dv: for every 128-key tile, loop over the 128-query tiles
+ * that see it, recompute S^T, P^T = exp(s K Q^T - LSE) and dP^T = V dO^T on
+ * chip, form dS^T = P^T * (dP^T - D), accumulate dV = P^T dO and
+ * dK = s dS^T Q on chip and write dk, dv (dtype).  No dQ work.
+ *
+ * fa_backward_dq: for every 128-query tile, loop over the key tiles it sees,
+ * recompute S, P and dP, form dS = P * (dP - D), accumulate dQ = s dS K on
+ * chip and write dq (dtype).  Writes nothing else; needs no workspace.
+ *
+ * Both: dense [B, H, N, d] tensors, d in {64, 96, 128} (256 gives
+ * FA_ERR_UNSUPPORTED), lse and delta [B, H, N] float32 inputs (the forward's
+ * LSE and the preprocess stage's D); causal: tiles entirely above the
+ * diagonal are skipped.  Errors as fa_backward_dkdv, before any launch.
+ */
+fa_status fa_backward_dk_dv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                            const float* delta, void* dk, void* dv, int B, int H, int N, int d, int dtype, int causal,
+                            float scale, void* stream);
+fa_status fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                         const float* delta, void* dq, int B, int H, int N, int d, int dtype, int causal, float scale,
+                         void* stream);
 
 /*
  * Packed variable-length batches.  B sequences of different lengths laid end
