@@ -14,9 +14,11 @@
 // fa_bwd_dkdv_split_kernel -- one CTA per 128-key tile (the MMA M dimension),
 // looping over 128-query tiles.  TMEM (D = 128):
 //   S^T 128 | dP^T 128 | dV 128 | dK 128   (D = 64: dV 64 | dK 64)
-//   S^T = K Q_i^T, dP^T = V dO_i^T;  P^T and dS^T are written as 16-bit pairs
-//   over the first half of each compute warpgroup's own S^T / dP^T columns,
-//   where dV += P^T dO_i and dK += dS^T Q_i read them as A operands.
+//   S^T = K Q_i^T, dP^T = V dO_i^T;  P^T goes to a shared-memory buffer (the
+//   A operand of dV += P^T dO_i), so S^T(i+1) can be computed as soon as the
+//   compute warps hold S^T(i) in registers; dS^T is written as 16-bit pairs
+//   over the first half of each compute warpgroup's own dP^T columns, where
+//   dK += dS^T Q_i reads it as a TMEM A operand.
 // Warps (384 threads):
 //   0      TMA: K, V once; Q_i, dO_i through a ring (2 stages at D = 128).
 //   1      TMEM allocation; lane 0 issues S^T(i+1) and dV(i).
@@ -24,21 +26,21 @@
 //   4-7 / 8-11  compute warpgroup h = 0 / 1: one key row per thread (TMEM
 //          lane), query columns [64h, 64h + 64): P^T from S^T and LSE (pass
 //          1, P kept in registers), then dS^T from dP^T and D (pass 2).
-//   Each issuer orders its own product pair: dV(i) reads P^T(i) from the S^T
-//   columns before S^T(i+1) overwrites them (same issuing thread, in order),
-//   and likewise dK(i) before dP^T(i+1).  P^T(i) is formed while dK(i-1) and
-//   dP^T(i) run, dS^T(i) while dV(i) and S^T(i+1) run.
+//   dK(i) reads dS^T(i) from the dP^T columns before dP^T(i+1) overwrites
+//   them (same issuing thread, in order).
 //
 // fa_bwd_dq_kernel -- one CTA per 128-query tile, looping over 128-key tiles.
-// Q and dO of the tile are copied once into TMEM as A operands.  TMEM (D = 128):
-//   Q 64 | dO 64 | S 128 | dP 128 | dQ 128
-//   S = Q K_j^T, dP = dO V_j^T;  dS (16-bit) over the first half of each
-//   compute warpgroup's dP columns;  dQ += dS K_j accumulates in TMEM for the
-//   whole key loop and is scaled and stored once.
-// Warps (384 threads): 0 TMA (Q, dO once; K_j, V_j through a 4-slot ring in
-//   the order K0 V0 K1 V1 ...), 1 TMEM allocation and the MMA issuer (order
-//   S(0) dP(0) | S(j+1) dQ(j) dP(j+1) | ...), 4-7 / 8-11 compute warpgroups,
-//   one query row per thread and key columns [64h, 64h + 64).
+// Q of the tile is copied once into TMEM as an A operand.  TMEM (D = 128):
+//   Q 64 | S 128 | dP 128 | dQ 128 | dS 64
+//   S = Q K_j^T (Q from TMEM), dP = dO V_j^T (dO from shared memory), dS
+//   (16-bit pairs), dQ += dS K_j accumulates in TMEM for the whole key loop
+//   and is scaled and stored once.
+// Warps (384 threads): 0 TMA (Q, dO once; K_j through a 3-slot ring, V_j
+//   through a 2-slot ring), 1 TMEM allocation and the issuer of S, 2 the
+//   issuer of dP (dO from shared memory), 3 the issuer of dQ, 4-7 / 8-11
+//   compute warpgroups, one query row per thread and key columns
+//   [64h, 64h + 64).  dS has TMEM columns of its own, so dP(j+1) never waits
+//   for dQ(j).
 //
 // Causal (square, top-left): query tiles entirely above the diagonal, and
 // key tiles entirely right of it, are skipped by the loop bounds (the
@@ -65,15 +67,24 @@ struct SplitCfg {
 template <int D>
 struct DkdvSplitCfg : SplitCfg<D> {
   using B = SplitCfg<D>;
+  // Of the 8 pairs of exponentials in a 16-column chunk, this many are
+  // evaluated on the FMA pipe (exp2_poly2), the rest on the special-function
+  // unit.
+  static constexpr int POLY_PAIRS = 0;
+  static constexpr int CWG = 4;                    // compute warpgroups, 32 query columns each
+  static constexpr int THREADS = 128 + 128 * CWG;
   static constexpr int QS = D == 128 ? 2 : 4;      // Q / dO stages
+  static constexpr int PT_SLAB = 128 * 128;        // 128 keys x 64 queries x 16 bit
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = B::TILE;
   static constexpr int OFF_Q = 2 * B::TILE;        // [QS]
   static constexpr int OFF_DO = OFF_Q + QS * B::TILE;
-  static constexpr int OFF_LD = OFF_DO + QS * B::TILE;  // [2 buffers][2: -LSE log2e, -D][128] floats
-  static constexpr int OFF_BAR = OFF_LD + 2 * 2 * 128 * 4;
-  // kv_full, q_full[QS], q_empty[QS], s_full, dp_full, p_full, ds_full, dkdv_done, drain[2], ld_full[2]
-  static constexpr int NBAR = 1 + 2 * QS + 5 + 2 + 2;
+  static constexpr int OFF_PT = OFF_DO + QS * B::TILE;  // P^T, 2 slabs (query halves), A operand of dV
+  static constexpr int OFF_LD = OFF_PT + 2 * PT_SLAB;   // [CWG][-LSE log2e, -D][32] floats
+  static constexpr int OFF_BAR = OFF_LD + CWG * 2 * 32 * 4;
+  // kv_full, q_full[QS], q_empty[QS], s_full, s_empty, p_full, pt_empty, dp_full, ds_full, dkdv_done,
+  // drain[2], ld_full[CWG], ld_empty[CWG]
+  static constexpr int NBAR = 1 + 2 * QS + 7 + 2 + 2 * CWG;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr uint32_t COL_S = 0;
@@ -85,7 +96,7 @@ struct DkdvSplitCfg : SplitCfg<D> {
 };
 
 template <int D, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     fa_bwd_dkdv_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                              const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
@@ -99,18 +110,22 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sDO = smem + C::OFF_DO;
+  uint8_t* sPT = smem + C::OFF_PT;
   float* sLD = reinterpret_cast<float*>(smem + C::OFF_LD);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* q_full = kv_full + 1;
   uint64_t* q_empty = q_full + C::QS;
   uint64_t* s_full = q_empty + C::QS;
-  uint64_t* dp_full = s_full + 1;
-  uint64_t* p_full = dp_full + 1;
-  uint64_t* ds_full = p_full + 1;
+  uint64_t* s_empty = s_full + 1;    // every compute warp holds S^T(i) in registers
+  uint64_t* p_full = s_empty + 1;    // P^T(i) written to shared memory
+  uint64_t* pt_empty = p_full + 1;   // dV(i) has read P^T(i)
+  uint64_t* dp_full = pt_empty + 1;
+  uint64_t* ds_full = dp_full + 1;   // dS^T(i) written over dP^T(i) in TMEM
   uint64_t* dkdv_done = ds_full + 1;
-  uint64_t* drain = dkdv_done + 1;
-  uint64_t* ld_full = drain + 2;  // [2]: -LSE log2e and -D of a tile staged by the compute warps
+  uint64_t* drain = dkdv_done + 1;   // [2]
+  uint64_t* ld_full = drain + 2;     // [CWG]
+  uint64_t* ld_empty = ld_full + C::CWG;  // [CWG]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -137,14 +152,17 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&q_empty[b], 2);  // dV (reads dO) and dK (reads Q) issuers
     }
     mbar_init(s_full, 1);
+    mbar_init(s_empty, 4 * C::CWG);   // every compute warp
+    mbar_init(p_full, 4 * C::CWG);
+    mbar_init(pt_empty, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 8);   // the 8 compute warps
-    mbar_init(ds_full, 8);
+    mbar_init(ds_full, 4 * C::CWG);
     mbar_init(dkdv_done, 2);
-    mbar_init(&drain[0], 1);
-    mbar_init(&drain[1], 1);
-    mbar_init(&ld_full[0], 8);
-    mbar_init(&ld_full[1], 8);
+    for (int b = 0; b < 2; ++b) mbar_init(&drain[b], 1);
+    for (int b = 0; b < C::CWG; ++b) {
+      mbar_init(&ld_full[b], 4);   // the 4 warps of a compute warpgroup
+      mbar_init(&ld_empty[b], 4);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -192,19 +210,20 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
-    //   warp 1: S^T(i) = K Q_i^T and dV += P^T(i) dO_i
-    //   warp 2: dP^T(i) = V dO_i^T and dK += dS^T(i) Q_i
+    //   warp 1: S^T(i) = K Q_i^T as soon as the compute warps hold S^T(i-1)
+    //           in registers, and dV += P^T(i) dO_i (P^T from shared memory)
+    //   warp 2: dP^T(i) = V dO_i^T and dK += dS^T(i) Q_i, dS^T read from the
+    //           dP^T columns it overwrote (so dK(i) precedes dP^T(i+1) on the
+    //           same issuing thread)
     if (lane == 0) {
       const bool first_pair = warp == 1;
       constexpr uint32_t kIdT = idesc_f16(128, C::BQ, BF16, false, false);  // K-major A and B
-      constexpr uint32_t kIdAcc = idesc_f16(128, D, BF16, false, true);    // A from TMEM, MN-major B
+      constexpr uint32_t kIdAcc = idesc_f16(128, D, BF16, false, true);    // K-major A, MN-major B
       const uint32_t aKV = smem_u32(first_pair ? sK : sV);
       const uint32_t aQD = smem_u32(first_pair ? sQ : sDO);   // B of S^T / dP^T
       const uint32_t aB2 = smem_u32(first_pair ? sDO : sQ);   // B of dV / dK
+      const uint32_t aPT = smem_u32(sPT);
       const uint32_t col_t = first_pair ? C::COL_S : C::COL_DP;
-      const uint32_t col_acc = first_pair ? C::COL_DV : C::COL_DK;
-      uint64_t* t_full = first_pair ? s_full : dp_full;
-      uint64_t* a_full = first_pair ? p_full : ds_full;
       auto issue_t = [&](int qs) {  // S^T or dP^T of the tile in stage qs
         const uint64_t da = sdesc_sw128(aKV, 16, 1024);
         const uint64_t db = sdesc_sw128(aQD + qs * C::TILE, 16, 1024);
@@ -214,14 +233,23 @@ __global__ void __launch_bounds__(384, 1)
           mma_ss(tmem + col_t, da + o, db + o, kIdT, kk > 0);
         }
       };
-      auto issue_acc = [&](int qs, bool first) {  // dV += P^T dO or dK += dS^T Q
+      auto issue_dv = [&](int qs, bool first) {  // dV += P^T dO, P^T from shared memory
+        const uint64_t da = sdesc_sw128(aPT, 16, 1024);
         const uint64_t db = sdesc_sw128(aB2 + qs * C::TILE, C::SLAB, 1024);
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk) {
-          // query columns 16kk .. 16kk+15: warpgroup kk/4 wrote them as 16-bit
+          const uint32_t oa = ((kk >> 2) * C::PT_SLAB + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_DV, da + oa, db + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
+        }
+      };
+      auto issue_dk = [&](int qs, bool first) {  // dK += dS^T Q, dS^T from TMEM
+        const uint64_t db = sdesc_sw128(aB2 + qs * C::TILE, C::SLAB, 1024);
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk) {
+          // query columns 16kk .. 16kk+15: warpgroup kk/2 wrote them as 16-bit
           // pairs from its first column, 8 columns per 16 queries
-          const uint32_t a = tmem + col_t + 64 * (kk >> 2) + 8 * (kk & 3);
-          mma_ts(tmem + col_acc, a, db + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
+          const uint32_t a = tmem + C::COL_DP + 32 * (kk >> 1) + 8 * (kk & 1);
+          mma_ts(tmem + C::COL_DK, a, db + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
         }
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag, status, kStatusTimeout);
@@ -230,21 +258,37 @@ __global__ void __launch_bounds__(384, 1)
         if (ok) {
           tc_fence_after();
           issue_t(0);
-          mma_commit(t_full);
+          mma_commit(first_pair ? s_full : dp_full);
         }
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int qs = it % C::QS;
-        if (!(ok = mbar_wait(a_full, it & 1, abort_flag, status, kStatusTimeout))) break;
-        tc_fence_after();
-        issue_acc(qs, it == 0);
-        mma_commit(&q_empty[qs]);
-        if (it + 1 < n_it) {
-          const int qn = (it + 1) % C::QS;
-          if (!(ok = mbar_wait(&q_full[qn], ((it + 1) / C::QS) & 1, abort_flag, status, kStatusTimeout))) break;
+        const int qn = (it + 1) % C::QS;
+        const uint32_t qpar = ((it + 1) / C::QS) & 1;
+        if (first_pair) {
+          if (it + 1 < n_it) {
+            if (!(ok = mbar_wait(s_empty, it & 1, abort_flag, status, kStatusTimeout))) break;
+            if (!(ok = mbar_wait(&q_full[qn], qpar, abort_flag, status, kStatusTimeout))) break;
+            tc_fence_after();
+            issue_t(qn);
+            mma_commit(s_full);
+          }
+          if (!(ok = mbar_wait(p_full, it & 1, abort_flag, status, kStatusTimeout))) break;
           tc_fence_after();
-          issue_t(qn);
-          mma_commit(t_full);
+          issue_dv(qs, it == 0);
+          mma_commit(pt_empty);
+          mma_commit(&q_empty[qs]);
+        } else {
+          if (!(ok = mbar_wait(ds_full, it & 1, abort_flag, status, kStatusTimeout))) break;
+          tc_fence_after();
+          issue_dk(qs, it == 0);
+          mma_commit(&q_empty[qs]);
+          if (it + 1 < n_it) {
+            if (!(ok = mbar_wait(&q_full[qn], qpar, abort_flag, status, kStatusTimeout))) break;
+            tc_fence_after();
+            issue_t(qn);
+            mma_commit(dp_full);
+          }
         }
       }
       if (ok) {
@@ -257,18 +301,25 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute: P^T, dS^T
-    const int h = (warp >> 2) - 1;  // query columns [64h, 64h + 64)
+    constexpr int QW = C::BQ / C::CWG;  // query columns per warpgroup
+    constexpr int NC = QW / 16;         // 16-column chunks per warpgroup
+    const int h = (warp >> 2) - 1;      // query columns [QW h, QW (h + 1))
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int key = kv0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
     const long long row0 = (long long)bh * N;
-    // -LSE*log2(e) and -D of query column 64h + r (r < 64), fetched one tile ahead
+    float* sNL = sLD + h * 2 * QW;  // this warpgroup's columns: -LSE log2e, then -D
+    float* sND = sNL + QW;
+    // P^T of this warpgroup's queries: slab (QW h) / 64, from column (QW h) % 64
+    uint8_t* ptslab = sPT + ((QW * h) / 64) * C::PT_SLAB;
+    const int ptcol = (QW * h) % 64;
+    // -LSE*log2(e) and -D of query column QW h + r (r < QW), fetched one tile ahead
     float pre_l = 0.f, pre_d = 0.f;
     auto fetch = [&](int i) {
-      const int q = i * C::BQ + 64 * h + r;
-      if (r < 64) {
+      const int q = i * C::BQ + QW * h + r;
+      if (r < QW) {
         if (q < N) {
           const float lq = lse[row0 + q];
           pre_l = lq == -pos_inf() ? -pos_inf() : -lq * kLog2e;
@@ -284,62 +335,76 @@ __global__ void __launch_bounds__(384, 1)
     for (int it = 0; it < n_it; ++it) {
       const int i = i_begin + it;
       const int q0 = i * C::BQ;
-      float* sNL = sLD + (it & 1) * 256;
-      float* sND = sNL + 128;
-      if (r < 64) {
-        sNL[64 * h + r] = pre_l;
-        sND[64 * h + r] = pre_d;
+      // the staged values of the previous tile have been read by every warp of the warpgroup
+      if (it > 0 && !(ok = warp_wait(&ld_empty[h], (it - 1) & 1, abort_flag, status))) break;
+      if (r < QW) {
+        sNL[r] = pre_l;
+        sND[r] = pre_d;
       }
-      // Buffer it & 1 is rewritten two tiles later, after every compute warp
-      // has passed this wait for the next tile, i.e. finished this one.
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ld_full[it & 1]);
-      if (!(ok = warp_wait(&ld_full[it & 1], (it >> 1) & 1, abort_flag, status))) break;
+      if (lane == 0) mbar_arrive(&ld_full[h]);
+      if (!(ok = warp_wait(&ld_full[h], it & 1, abort_flag, status))) break;
       if (it + 1 < n_it) fetch(i + 1);
-      // ---- pass 1: P^T = exp2(S^T s log2e - LSE log2e), masked
+      // ---- pass 1: S^T into registers (S^T(i+1) may then be issued), P^T into shared memory
       if (!(ok = warp_wait(s_full, it & 1, abort_flag, status))) break;
       tc_fence_after();
-      float p[4][16];
+      float p[NC][16];
 #pragma unroll
-      for (int sc = 0; sc < 4; ++sc) {
-        const int col = 64 * h + 16 * sc;  // first query column (within the tile) of this chunk
-        float s[16];
-        tmem_ld16(lane_base + C::COL_S + col, s);
-        tmem_ld_wait(s);
-        const int c0 = q0 + col;
+      for (int sc = 0; sc < NC; ++sc) tmem_ld16(lane_base + C::COL_S + QW * h + 16 * sc, p[sc]);
+#pragma unroll
+      for (int sc = 0; sc < NC; ++sc) tmem_ld_wait(p[sc]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      uint32_t pk[NC][8];
+#pragma unroll
+      for (int sc = 0; sc < NC; ++sc) {
+        const int col = 16 * sc;  // first query column of this chunk within the warpgroup's columns
+        const int c0 = q0 + QW * h + col;
         const bool need_mask = (CAUSAL && c0 < kv0 + C::BKV - 1) || (kv0 + C::BKV > N);
-        uint32_t pk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int c = 2 * e;
           const float2 nl = *reinterpret_cast<const float2*>(sNL + col + c);
           float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, f2_pack(nl.x, nl.y)), x0, x1);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
+          f2_unpack(f2_fma(f2_pack(p[sc][c], p[sc][c + 1]), sc2, f2_pack(nl.x, nl.y)), x0, x1);
+          float p0, p1;
+          if (e < C::POLY_PAIRS) {
+            exp2_poly2(x0, x1, p0, p1);
+            if (nl.x == -pos_inf()) p0 = 0.f;  // padding query (2^-125, not 0, from the polynomial)
+            if (nl.y == -pos_inf()) p1 = 0.f;
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
           if (need_mask) {
             if (key >= N || (CAUSAL && key > c0 + c)) p0 = 0.f;
             if (key >= N || (CAUSAL && key > c0 + c + 1)) p1 = 0.f;
           }
           p[sc][c] = p0;
           p[sc][c + 1] = p1;
-          pk[e] = pack2(p0, p1, BF16);
+          pk[sc][e] = pack2(p0, p1, BF16);
         }
-        // columns [col/2 ...] of this warpgroup's own half were read in chunk sc/2 <= sc
-        tmem_st8(lane_base + C::COL_S + 64 * h + 8 * sc, pk);
       }
-      tmem_st_wait();
-      tc_fence_before();
+      // the P^T buffer is free once dV(i-1) has read it
+      if (it > 0 && !(ok = warp_wait(pt_empty, (it - 1) & 1, abort_flag, status))) break;
+#pragma unroll
+      for (int sc = 0; sc < NC; ++sc)
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          *reinterpret_cast<uint4*>(ptslab + sw128_offset(r, ptcol + 16 * sc + 8 * u)) =
+              make_uint4(pk[sc][4 * u], pk[sc][4 * u + 1], pk[sc][4 * u + 2], pk[sc][4 * u + 3]);
+      fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
-      // ---- pass 2: dS^T = P^T * (dP^T - D)
+      // ---- pass 2: dS^T = P^T * (dP^T - D), written over dP^T
       if (!(ok = warp_wait(dp_full, it & 1, abort_flag, status))) break;
       tc_fence_after();
 #pragma unroll
-      for (int sc = 0; sc < 4; ++sc) {
-        const int col = 64 * h + 16 * sc;
+      for (int sc = 0; sc < NC; ++sc) {
+        const int col = 16 * sc;
         float dp[16];
-        tmem_ld16(lane_base + C::COL_DP + col, dp);
+        tmem_ld16(lane_base + C::COL_DP + QW * h + col, dp);
         tmem_ld_wait(dp);
         uint32_t dk[8];
 #pragma unroll
@@ -351,26 +416,38 @@ __global__ void __launch_bounds__(384, 1)
           f2_unpack(f2_mul(f2_pack(p[sc][c], p[sc][c + 1]), t2), d0, d1);
           dk[e] = pack2(d0, d1, BF16);
         }
-        tmem_st8(lane_base + C::COL_DP + 64 * h + 8 * sc, dk);
+        // columns [QW h + col/2, +8) of this warpgroup's own columns were read in chunk sc/2 <= sc
+        tmem_st8(lane_base + C::COL_DP + QW * h + 8 * sc, dk);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) {
+        mbar_arrive(ds_full);
+        mbar_arrive(&ld_empty[h]);
+      }
     }
     // ------------------------------------------------------------ epilogue
-    // dV (warpgroup 0, staged in the Q stages) and dK * scale (warpgroup 1,
-    // staged in the dO stages), stored with TMA; rows past N and features
-    // past dh fall outside the tensor maps.  Every warp reaches the barrier.
+    // Warpgroups 0 and 1 stage the two 64-feature halves of dV in the Q
+    // stages, warpgroups 2 and 3 those of dK * scale in the dO stages; each
+    // stores its slab with TMA (rows past N and features past dh fall outside
+    // the tensor maps).  Every warp reaches its warpgroup's barrier once.
+    const bool is_dk = h >= 2;
+    const int half = h & 1;
+    const bool has_half = 64 * half < D;
     if (ok && n_it > 0) ok = warp_wait(dkdv_done, 0, abort_flag, status);
     if (ok) tc_fence_after();
-    uint8_t* stage = h == 0 ? sQ : sDO;
-    if (ok) stage_rows_from_tmem<D, BF16>(lane_base + (h == 0 ? C::COL_DV : C::COL_DK), stage, r,
-                                          h == 0 ? 1.f : scale, n_it == 0);
+    uint8_t* stage = (is_dk ? sDO : sQ) + half * C::SLAB;
+    if (ok && has_half)
+      stage_rows_from_tmem<64, BF16>(lane_base + (is_dk ? C::COL_DK : C::COL_DV) + 64 * half, stage, r,
+                                     is_dk ? scale : 1.f, n_it == 0);
     fence_async_smem();
     named_barrier_sync(1 + h, 128);
-    if (r == 0 && ok && !*abort_flag)
-      store_staged_tile<D>(h == 0 ? &tm_dv : &tm_dk, stage, 0, dh, make_int2(kv0, bh));
+    if (r == 0 && ok && has_half && !*abort_flag && 64 * half < dh) {
+      tma_store_3d(is_dk ? &tm_dk : &tm_dv, stage, 64 * half, kv0, bh);
+      tma_store_commit();
+      tma_store_wait_read();
+    }
   }
 
   tc_fence_before();
@@ -385,26 +462,34 @@ __global__ void __launch_bounds__(384, 1)
 template <int D>
 struct DqCfg : SplitCfg<D> {
   using B = SplitCfg<D>;
-  static constexpr int NS = D == 128 ? 4 : 8;      // K / V ring slots
-  static constexpr int OFF_RING = 0;
-  static constexpr int OFF_Q = NS * B::TILE;       // Q and dO staging (copied into TMEM once)
-  static constexpr int OFF_DO = OFF_Q + B::TILE;
+  static constexpr int POLY_PAIRS = 0;  // as DkdvSplitCfg
+  static constexpr int CWG = 4;         // compute warpgroups, 32 key columns each
+  static constexpr int THREADS = 128 + 128 * CWG;
+  // K_j is read by S(j) and, a tile later, by dQ(j); V_j only by dP(j): K
+  // and V have rings of their own so that a K slot held until dQ(j) never
+  // delays the next tiles' loads.
+  static constexpr int NK = 3;                     // K ring slots
+  static constexpr int NV = 2;                     // V ring slots (slot 1 first stages Q)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = NK * B::TILE;
+  static constexpr int OFF_DO = OFF_V + NV * B::TILE;  // dO, the A operand of dP for the whole CTA
   static constexpr int OFF_BAR = OFF_DO + B::TILE;
-  // q_full, qa_full, ring_full[NS], ring_empty[NS], s_full, s_empty, dp_full, ds_full, dq_full, drain
-  static constexpr int NBAR = 2 + 2 * NS + 6;
+  // q_full, qa_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full, s_empty, dp_full, dp_empty,
+  // ds_full, ds_empty, dq_full, drain[3]
+  static constexpr int NBAR = 2 + 2 * NK + 2 * NV + 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr uint32_t COL_QA = 0;            // Q as 16-bit pairs (A operand), D/2 columns
-  static constexpr uint32_t COL_DOA = D / 2;       // dO likewise
-  static constexpr uint32_t COL_S = D;             // 128
-  static constexpr uint32_t COL_DP = D + 128;      // 128
-  static constexpr uint32_t COL_DQ = D + 256;      // D
-  static_assert(COL_DQ + D <= B::TMEM_COLS, "TMEM budget");
+  static constexpr uint32_t COL_S = 64;            // 128
+  static constexpr uint32_t COL_DP = 192;          // 128
+  static constexpr uint32_t COL_DQ = 320;          // D
+  static constexpr uint32_t COL_DS = 320 + D;      // dS as 16-bit pairs (A operand of dQ), 64 columns
+  static_assert(COL_DS + 64 <= B::TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 template <int D, bool CAUSAL, bool BF16>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      void* __restrict__ dq, const float* __restrict__ lse, const float* __restrict__ delta, int N,
@@ -413,20 +498,25 @@ __global__ void __launch_bounds__(384, 1)
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sRing = smem + C::OFF_RING;
-  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sQ = sV + C::TILE;  // Q staging in V slot 1 until V_1 is loaded
   uint8_t* sDO = smem + C::OFF_DO;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* qa_full = q_full + 1;
-  uint64_t* ring_full = qa_full + 1;
-  uint64_t* ring_empty = ring_full + C::NS;
-  uint64_t* s_full = ring_empty + C::NS;
-  uint64_t* s_empty = s_full + 1;
+  uint64_t* k_full = qa_full + 1;
+  uint64_t* k_empty = k_full + C::NK;
+  uint64_t* v_full = k_empty + C::NK;
+  uint64_t* v_empty = v_full + C::NV;
+  uint64_t* s_full = v_empty + C::NV;
+  uint64_t* s_empty = s_full + 1;    // every compute warp holds S(j) in registers
   uint64_t* dp_full = s_empty + 1;
-  uint64_t* ds_full = dp_full + 1;
-  uint64_t* dq_full = ds_full + 1;
-  uint64_t* drain = dq_full + 1;
+  uint64_t* dp_empty = dp_full + 1;  // every compute warp holds dP(j) (as dS) in registers
+  uint64_t* ds_full = dp_empty + 1;  // dS(j) written to its TMEM columns
+  uint64_t* ds_empty = ds_full + 1;  // dQ(j) has read dS(j)
+  uint64_t* dq_full = ds_empty + 1;
+  uint64_t* drain = dq_full + 1;     // [3]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -445,17 +535,23 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(qa_full, 8);  // the 8 compute warps
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&ring_full[s], 1);
-      mbar_init(&ring_empty[s], 1);
+    mbar_init(qa_full, 4);  // the 4 warps of compute warpgroup 0
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_empty, 8);
+    mbar_init(s_empty, 4 * C::CWG);  // every compute warp
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 8);
+    mbar_init(dp_empty, 4 * C::CWG);
+    mbar_init(ds_full, 4 * C::CWG);
+    mbar_init(ds_empty, 1);
     mbar_init(dq_full, 1);
-    mbar_init(drain, 1);
+    for (int b = 0; b < 3; ++b) mbar_init(&drain[b], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -482,125 +578,121 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(sQ + s * C::SLAB, &tm_q, q_full, s * 64, q0, bh);
         tma_load_3d(sDO + s * C::SLAB, &tm_do, q_full, s * 64, q0, bh);
       }
-      int issued = 0;
-      for (int u = 0; u < 2 * n; ++u) {  // K_0, V_0, K_1, V_1, ...
-        const int slot = u % C::NS;
-        const uint32_t use = (uint32_t)(u / C::NS);
-        if (!mbar_wait(&ring_empty[slot], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
-        mbar_arrive_expect_tx(&ring_full[slot], C::TILE);
-        const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
+      int k_issued = 0, v_issued = 0;
+      for (int jt = 0; jt < n; ++jt) {  // K_0, V_0, K_1, V_1, ...
+        const int ks = jt % C::NK, vs = jt % C::NV;
+        if (!mbar_wait(&k_empty[ks], ((jt / C::NK) & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
+        mbar_arrive_expect_tx(&k_full[ks], C::TILE);
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, m, &ring_full[slot], s * 64, (u >> 1) * C::BKV, bh);
-        issued = u + 1;
+          tma_load_3d(sK + ks * C::TILE + s * C::SLAB, &tm_k, &k_full[ks], s * 64, jt * C::BKV, bh);
+        k_issued = jt + 1;
+        // V slot 1 holds the staged Q until warpgroup 0 has copied it into TMEM
+        if (jt == 1 && !mbar_wait(qa_full, 0, abort_flag, status, kStatusTimeout)) break;
+        if (!mbar_wait(&v_empty[vs], ((jt / C::NV) & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
+        mbar_arrive_expect_tx(&v_full[vs], C::TILE);
+        for (int s = 0; s < C::SLABS; ++s)
+          tma_load_3d(sV + vs * C::TILE + s * C::SLAB, &tm_v, &v_full[vs], s * 64, jt * C::BKV, bh);
+        v_issued = jt + 1;
       }
       if (*abort_flag) {
         drain_wait(q_full, 0);
-        for (int u = issued - C::NS < 0 ? 0 : issued - C::NS; u < issued; ++u)
-          drain_wait(&ring_full[u % C::NS], (uint32_t)((u / C::NS) & 1));
+        for (int jt = k_issued - C::NK < 0 ? 0 : k_issued - C::NK; jt < k_issued; ++jt)
+          drain_wait(&k_full[jt % C::NK], (uint32_t)((jt / C::NK) & 1));
+        for (int jt = v_issued - C::NV < 0 ? 0 : v_issued - C::NV; jt < v_issued; ++jt)
+          drain_wait(&v_full[jt % C::NV], (uint32_t)((jt / C::NV) & 1));
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= 1 && warp <= 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread issues about one MMA per ~100 cycles, so each product has
+    // a thread of its own:
+    //   warp 1: S(j) = Q K_j^T (Q from TMEM) once S(j-1) is in registers
+    //   warp 2: dP(j) = dO V_j^T (dO from shared memory) once dP(j-1) is
+    //   warp 3: dQ += dS(j) K_j once dS(j) is written (dS from TMEM)
     if (lane == 0) {
-      constexpr uint32_t kIdT = idesc_f16(128, C::BKV, BF16, false, false);  // A from TMEM, K-major B
+      constexpr uint32_t kIdT = idesc_f16(128, C::BKV, BF16, false, false);  // K-major A and B
       constexpr uint32_t kIdDq = idesc_f16(128, D, BF16, false, true);       // A from TMEM, MN-major B
-      const uint32_t ring = smem_u32(sRing);
-      auto slot_of = [](int u) { return u % C::NS; };
-      auto par_of = [](int u) { return (uint32_t)((u / C::NS) & 1); };
-      // S = Q K_j^T (a = Q) or dP = dO V_j^T (a = dO): tile item u of the ring
-      auto issue_t = [&](uint32_t acol, uint32_t dcol, int u) {
-        const uint64_t db = sdesc_sw128(ring + slot_of(u) * C::TILE, 16, 1024);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      const uint32_t aDO = smem_u32(sDO);
+      bool ok = true;
+      if (warp == 1) {
+        ok = mbar_wait(qa_full, 0, abort_flag, status, kStatusTimeout);
+        for (int jt = 0; ok && jt < n; ++jt) {
+          if (jt > 0 && !(ok = mbar_wait(s_empty, (jt - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+          if (!(ok = mbar_wait(&k_full[jt % C::NK], (jt / C::NK) & 1, abort_flag, status, kStatusTimeout))) break;
+          tc_fence_after();
+          const uint64_t db = sdesc_sw128(aK + (jt % C::NK) * C::TILE, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = ((kk >> 2) * C::SLAB + (kk & 3) * 32) >> 4;
-          mma_ts(tmem + dcol, tmem + acol + 8 * kk, db + o, kIdT, kk > 0);
-        }
-      };
-      auto issue_dq = [&](int u, bool first) {  // dQ += dS K_j
-        const uint64_t db = sdesc_sw128(ring + slot_of(u) * C::TILE, C::SLAB, 1024);
-#pragma unroll
-        for (int kk = 0; kk < C::BKV / 16; ++kk) {
-          const uint32_t a = tmem + C::COL_DP + 64 * (kk >> 2) + 8 * (kk & 3);
-          mma_ts(tmem + C::COL_DQ, a, db + ((kk * 2048) >> 4), kIdDq, !(first && kk == 0));
-        }
-      };
-      bool ok = mbar_wait(qa_full, 0, abort_flag, status, kStatusTimeout);
-      if (ok && n > 0) {
-        ok = mbar_wait(&ring_full[slot_of(0)], par_of(0), abort_flag, status, kStatusTimeout);
-        if (ok) {
-          tc_fence_after();
-          issue_t(C::COL_QA, C::COL_S, 0);
-          mma_commit(s_full);
-          ok = mbar_wait(&ring_full[slot_of(1)], par_of(1), abort_flag, status, kStatusTimeout);
-        }
-        if (ok) {
-          tc_fence_after();
-          issue_t(C::COL_DOA, C::COL_DP, 1);
-          mma_commit(dp_full);
-          mma_commit(&ring_empty[slot_of(1)]);
-        }
-      }
-      for (int jt = 0; ok && jt < n; ++jt) {
-        if (jt + 1 < n) {  // S(j+1) once the compute warps hold S(j) in registers
-          if (!(ok = mbar_wait(s_empty, jt & 1, abort_flag, status, kStatusTimeout))) break;
-          if (!(ok = mbar_wait(&ring_full[slot_of(2 * jt + 2)], par_of(2 * jt + 2), abort_flag, status,
-                               kStatusTimeout)))
-            break;
-          tc_fence_after();
-          issue_t(C::COL_QA, C::COL_S, 2 * jt + 2);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = ((kk >> 2) * C::SLAB + (kk & 3) * 32) >> 4;
+            mma_ts(tmem + C::COL_S, tmem + C::COL_QA + 8 * kk, db + o, kIdT, kk > 0);
+          }
           mma_commit(s_full);
         }
-        if (!(ok = mbar_wait(ds_full, jt & 1, abort_flag, status, kStatusTimeout))) break;
-        tc_fence_after();
-        issue_dq(2 * jt, jt == 0);
-        mma_commit(&ring_empty[slot_of(2 * jt)]);
-        if (jt + 1 < n) {  // dP(j+1) overwrites dS(j) after dQ(j) has read it (same thread, in order)
-          if (!(ok = mbar_wait(&ring_full[slot_of(2 * jt + 3)], par_of(2 * jt + 3), abort_flag, status,
-                               kStatusTimeout)))
-            break;
+      } else if (warp == 2) {
+        ok = mbar_wait(q_full, 0, abort_flag, status, kStatusTimeout);
+        for (int jt = 0; ok && jt < n; ++jt) {
+          if (jt > 0 && !(ok = mbar_wait(dp_empty, (jt - 1) & 1, abort_flag, status, kStatusTimeout))) break;
+          if (!(ok = mbar_wait(&v_full[jt % C::NV], (jt / C::NV) & 1, abort_flag, status, kStatusTimeout))) break;
           tc_fence_after();
-          issue_t(C::COL_DOA, C::COL_DP, 2 * jt + 3);
+          const uint64_t da = sdesc_sw128(aDO, 16, 1024);
+          const uint64_t db = sdesc_sw128(aV + (jt % C::NV) * C::TILE, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = ((kk >> 2) * C::SLAB + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::COL_DP, da + o, db + o, kIdT, kk > 0);
+          }
           mma_commit(dp_full);
-          mma_commit(&ring_empty[slot_of(2 * jt + 3)]);
+          mma_commit(&v_empty[jt % C::NV]);
         }
-      }
-      if (ok) {
-        mma_commit(dq_full);
       } else {
-        mma_commit(drain);
-        drain_wait(drain, 0);
+        for (int jt = 0; ok && jt < n; ++jt) {
+          if (!(ok = mbar_wait(ds_full, jt & 1, abort_flag, status, kStatusTimeout))) break;
+          tc_fence_after();
+          const uint64_t db = sdesc_sw128(aK + (jt % C::NK) * C::TILE, C::SLAB, 1024);
+#pragma unroll
+          for (int kk = 0; kk < C::BKV / 16; ++kk)
+            mma_ts(tmem + C::COL_DQ, tmem + C::COL_DS + 8 * kk, db + ((kk * 2048) >> 4), kIdDq, !(jt == 0 && kk == 0));
+          mma_commit(ds_empty);
+          mma_commit(&k_empty[jt % C::NK]);  // K_j: S(j) finished before dS(j) existed
+        }
+        if (ok) mma_commit(dq_full);
+      }
+      if (!ok) {  // every MMA this thread issued must finish before TMEM is freed
+        mma_commit(&drain[warp - 1]);
+        drain_wait(&drain[warp - 1], 0);
       }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute: P, dS
-    const int h = (warp >> 2) - 1;  // key columns [64h, 64h + 64) of every tile
+    constexpr int KW = C::BKV / C::CWG;  // key columns per warpgroup
+    constexpr int NC = KW / 16;          // 16-column chunks per warpgroup
+    const int h = (warp >> 2) - 1;       // key columns [KW h, KW (h + 1)) of every tile
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int q = q0 + r;            // this thread's query row (TMEM lane)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     bool ok = true;
-    // Q (warpgroup 0) or dO (warpgroup 1) of this row into TMEM as 16-bit pairs.
-    if (!(ok = warp_wait(q_full, 0, abort_flag, status))) {
-    } else {
-      const uint8_t* src = h == 0 ? sQ : sDO;
-      const uint32_t dcol = h == 0 ? C::COL_QA : C::COL_DOA;
+    if (h == 0) {  // Q of this row into TMEM as 16-bit pairs (the A operand of S)
+      if ((ok = warp_wait(q_full, 0, abort_flag, status))) {
 #pragma unroll
-      for (int s = 0; s < C::SLABS; ++s) {
-        uint32_t v[32];
+        for (int s = 0; s < C::SLABS; ++s) {
+          uint32_t v[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 x = *reinterpret_cast<const uint4*>(src + s * C::SLAB + sw128_offset(r, 8 * u));
-          v[4 * u] = x.x;
-          v[4 * u + 1] = x.y;
-          v[4 * u + 2] = x.z;
-          v[4 * u + 3] = x.w;
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = *reinterpret_cast<const uint4*>(sQ + s * C::SLAB + sw128_offset(r, 8 * u));
+            v[4 * u] = x.x;
+            v[4 * u + 1] = x.y;
+            v[4 * u + 2] = x.z;
+            v[4 * u + 3] = x.w;
+          }
+          tmem_st32(lane_base + C::COL_QA + 32 * s, v);
         }
-        tmem_st32(lane_base + dcol + 32 * s, v);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qa_full);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qa_full);
     }
     const long long frow = (long long)bh * N + q;
     float nl = -pos_inf(), nd = 0.f;  // padding rows: P = 0
@@ -613,27 +705,33 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t nl2 = f2_pack(nl, nl);
     const uint64_t nd2 = f2_pack(nd, nd);
     for (int jt = 0; ok && jt < n; ++jt) {
-      const int kb = jt * C::BKV + 64 * h;  // first key of this warpgroup's columns
+      const int kb = jt * C::BKV + KW * h;  // first key of this warpgroup's columns
       if (!(ok = warp_wait(s_full, jt & 1, abort_flag, status))) break;
       tc_fence_after();
-      float p[4][16];
+      float p[NC][16];
 #pragma unroll
-      for (int sc = 0; sc < 4; ++sc) tmem_ld16(lane_base + C::COL_S + 64 * h + 16 * sc, p[sc]);
+      for (int sc = 0; sc < NC; ++sc) tmem_ld16(lane_base + C::COL_S + KW * h + 16 * sc, p[sc]);
 #pragma unroll
-      for (int sc = 0; sc < 4; ++sc) tmem_ld_wait(p[sc]);
+      for (int sc = 0; sc < NC; ++sc) tmem_ld_wait(p[sc]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty);
 #pragma unroll
-      for (int sc = 0; sc < 4; ++sc) {
+      for (int sc = 0; sc < NC; ++sc) {
         const int k0 = kb + 16 * sc;
         const bool need_mask = (CAUSAL && k0 + 15 > q0) || (k0 + 16 > N);
 #pragma unroll
         for (int c = 0; c < 16; c += 2) {
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(p[sc][c], p[sc][c + 1]), sc2, nl2), x0, x1);
-          float p0 = ex2_approx(x0);
-          float p1 = ex2_approx(x1);
+          float p0, p1;
+          if ((c >> 1) < C::POLY_PAIRS) {
+            exp2_poly2(x0, x1, p0, p1);
+            if (q >= N) p0 = p1 = 0.f;  // padding rows (the polynomial gives 2^-125, not 0, at -inf)
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
           if (need_mask) {
             if (k0 + c >= N || (CAUSAL && k0 + c > q)) p0 = 0.f;
             if (k0 + c + 1 >= N || (CAUSAL && k0 + c + 1 > q)) p1 = 0.f;
@@ -644,22 +742,29 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!(ok = warp_wait(dp_full, jt & 1, abort_flag, status))) break;
       tc_fence_after();
+      uint32_t pk[NC][8];
 #pragma unroll
-      for (int sc = 0; sc < 4; ++sc) {
+      for (int sc = 0; sc < NC; ++sc) {
         float dp[16];
-        tmem_ld16(lane_base + C::COL_DP + 64 * h + 16 * sc, dp);
+        tmem_ld16(lane_base + C::COL_DP + KW * h + 16 * sc, dp);
         tmem_ld_wait(dp);
-        uint32_t pk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           float d0, d1;
           f2_unpack(f2_mul(f2_pack(p[sc][2 * e], p[sc][2 * e + 1]), f2_add(f2_pack(dp[2 * e], dp[2 * e + 1]), nd2)),
                     d0, d1);
-          pk[e] = pack2(d0, d1, BF16);
+          pk[sc][e] = pack2(d0, d1, BF16);
         }
-        // the columns written were read in chunk sc/2 <= sc
-        tmem_st8(lane_base + C::COL_DP + 64 * h + 8 * sc, pk);
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dp_empty);
+      // the dS columns are free once dQ(j-1) has read them
+      if (jt > 0 && !(ok = warp_wait(ds_empty, (jt - 1) & 1, abort_flag, status))) break;
+      tc_fence_after();
+      // keys [KW h + 16 sc, +16) -> 16-bit pairs in columns COL_DS + KW h / 2 + 8 sc
+#pragma unroll
+      for (int sc = 0; sc < NC; ++sc) tmem_st8(lane_base + C::COL_DS + (KW / 2) * h + 8 * sc, pk[sc]);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -667,25 +772,25 @@ __global__ void __launch_bounds__(384, 1)
     }
     // ------------------------------------------------------------ epilogue
     // dQ = scale * (dS K summed over key tiles): warpgroup h writes features
-    // [D/2 h, D/2 (h + 1)) of its row, those below dh.
+    // [FW h, FW (h + 1)) of its row, those below dh.
+    constexpr int FW = D / C::CWG;
     if (ok) ok = warp_wait(dq_full, 0, abort_flag, status);
-    if (ok && n > 0) {
+    if (ok && n > 0 && FW * h < dh) {
       tc_fence_after();
-      uint4* drow = reinterpret_cast<uint4*>(dq) + frow * (dh / 8);
+      uint4* drow = reinterpret_cast<uint4*>(dq) + frow * (dh / 8) + FW * h / 8;
+      float v[FW];
+      if constexpr (FW == 32) {
+        tmem_ld32(lane_base + C::COL_DQ + FW * h, v);
+      } else {
+        tmem_ld16(lane_base + C::COL_DQ + FW * h, v);
+      }
+      tmem_ld_wait(v);
+      uint32_t pk[FW / 2];
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int f0 = (D / 2) * h + 32 * c;  // first feature of this 32-column chunk
-        if (f0 >= dh) break;
-        float v[32];
-        tmem_ld32(lane_base + C::COL_DQ + f0, v);
-        tmem_ld_wait(v);
-        uint32_t pk[16];
+      for (int e = 0; e < FW / 2; ++e) pk[e] = pack2(v[2 * e] * scale, v[2 * e + 1] * scale, BF16);
+      if (q < N) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack2(v[2 * e] * scale, v[2 * e + 1] * scale, BF16);
-        if (q < N) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) drow[f0 / 8 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
+        for (int u = 0; u < FW / 8; ++u) drow[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
     }
   }

@@ -285,6 +285,32 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 2^x for a packed pair, evaluated on the FMA and integer pipes instead of
+// the special-function unit (whose exponentials set the pace of the
+// backward's recompute of P): Cody and Waite's range reduction (W. J. Cody,
+// W. Waite, "Software Manual for the Elementary Functions", 1980),
+//   x = n + f,  n = round(x) (the 1.5 * 2^23 rounding trick),  f in [-1/2, 1/2],
+//   2^x = 2^f * 2^n,  2^n added into the exponent field,
+// with 2^f by a cubic fitted to 2^f on [-1/2, 1/2] in relative error
+// (iteratively reweighted least squares; max relative error 7.5e-5, below the
+// rounding of P to 16 bits).  Domain: x <= 127; x is clamped below at -125
+// (results under 2^-125, including x = -inf, come out as about 2^-125).
+__device__ __forceinline__ void exp2_poly2(float x0, float x1, float& y0, float& y1) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  const uint64_t x = f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
+  const uint64_t t = f2_add(x, f2_pack(kRound, kRound));                // low mantissa bits hold n
+  const uint64_t n = f2_add(t, f2_pack(-kRound, -kRound));              // n as a float
+  const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), x);                 // x - n
+  uint64_t p = f2_fma(f, f2_pack(0.0551716685f, 0.0551716685f), f2_pack(0.242611140f, 0.242611140f));
+  p = f2_fma(p, f, f2_pack(0.693260968f, 0.693260968f));
+  p = f2_fma(p, f, f2_pack(0.999928057f, 0.999928057f));
+  float p0, p1, t0, t1;
+  f2_unpack(p, p0, p1);
+  f2_unpack(t, t0, t1);
+  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+}
+
 // Byte offset of element (row, col) in a 128-byte-swizzled slab of 64
 // 16-bit columns (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B when
 // the slab starts on a 1024-byte boundary).
