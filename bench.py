@@ -1,9 +1,9 @@
 """Benchmark of the exact-attention hot path on GB300.
 
 One step = forward + backward (fa_forward, then the three backward stages
-fa_backward runs: preprocess, dK/dV, dQ convert) over one batch of the
-workload, by default the causal N=8192, d=128, bf16, B=2, H=32 problem.
-Prints ONE JSON line (rank 0).
+fa_backward runs for dense d <= 128: preprocess, dK/dV, dQ) over one batch
+of the workload, by default the causal N=8192, d=128, bf16, B=2, H=32
+problem.  Prints ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C4]
     python bench.py --impl reference ...   # the float64 CPU oracle as the baseline arm
@@ -30,10 +30,42 @@ if ROOT not in sys.path:
 
 METRIC = "attention TFLOPS (fwd, fwd+bwd) & % of GB300 dense BF16 tensor peak, N=4K–32K"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) of one dK/dV launch on C4, from an ncu capture of the current
-# kernel (dram__bytes_read.sum + dram__bytes_write.sum).  Reset to None whenever that kernel
-# changes, until a new capture is taken.
-DKDV_TRAFFIC_C4 = 832225024 + 510829568
+# The ncu capture of the roofline kernel (one C4 launch): its summary under profiles/ records
+# dram__bytes_read.sum + dram__bytes_write.sum per launch and a hash of the kernel's source
+# files at capture time; the bench reports that traffic only while the sources still hash the
+# same (a changed kernel reports null until it is captured again).
+DKDV_PROFILE = os.path.join(ROOT, "profiles", "fa_bwd_dkdv_split_C4_causal_n8192_d128_bf16.md")
+DKDV_SOURCES = ("fa_bwd_split.cu", "fa_bwd_kernel.cuh", "fa_ptx.cuh", "fa_internal.h", "fa_layout.cuh",
+                "fa_philox.cuh")
+
+
+def kernel_source_hash(names=DKDV_SOURCES) -> str:
+    """First 16 hex digits of the sha256 of the named csrc files, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "exact_io_aware_forward_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(path=DKDV_PROFILE):
+    """(bytes per launch, note) from a profile summary's `traffic_bytes_per_launch:` and
+    `source_sha256_16:` lines; bytes is None when absent or taken on other sources."""
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None, "no capture"
+    vals = {}
+    for line in text.splitlines():
+        for key in ("traffic_bytes_per_launch", "source_sha256_16"):
+            if line.strip().startswith(key + ":"):
+                vals[key] = line.split(":", 1)[1].strip().strip("`")
+    if "traffic_bytes_per_launch" not in vals or "source_sha256_16" not in vals:
+        return None, "capture lacks traffic or hash"
+    if vals["source_sha256_16"] != kernel_source_hash():
+        return None, "kernel changed since the capture"
+    return int(vals["traffic_bytes_per_launch"]), os.path.relpath(path, ROOT)
 
 
 def load_peaks():
@@ -399,8 +431,12 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
         else:
             fa.fa_forward_dropout(q, k, v, o, lse, DROP_P, DROP_SEED, DROP_OFFSET, w.causal)
 
+    split = kind == "dense" and d != 256  # the strategy fa_backward takes
+
     def dkdv():
-        if kind == "dense":
+        if split:
+            fa.fa_backward_dk_dv(q, k, v, do, lse, delta, dk, dv, w.causal)
+        elif kind == "dense":
             fa.fa_backward_dkdv(q, k, v, do, lse, delta, acc, dk, dv, w.causal)
         elif kind == "blocksparse":
             fa.fa_backward_dkdv_blocksparse(q, k, v, do, lse, delta, acc, dk, dv, md, w.causal)
@@ -415,11 +451,14 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
         fwd()
         if e: e[1].record(stream)
         fa.fa_backward_preprocess(flat(o), flat(do), delta.view(1, 1, rows) if kind == "varlen" else delta,
-                                  flat(acc))
+                                  None if split else flat(acc))
         if e: e[2].record(stream)
         dkdv()
         if e: e[3].record(stream)
-        fa.fa_backward_dq_convert(flat(acc), flat(dq), scale=1.0 / math.sqrt(d))
+        if split:
+            fa.fa_backward_dq(q, k, v, do, lse, delta, dq, w.causal)
+        else:
+            fa.fa_backward_dq_convert(flat(acc), flat(dq), scale=1.0 / math.sqrt(d))
         if e: e[4].record(stream)
 
     for _ in range(warmup):
@@ -440,6 +479,13 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
     parts = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps for j in range(4)]
     extra = (cu_q, cu_k) if kind == "varlen" else md
     return t0.elapsed_time(t1) / steps, parts, clocks, (q, k, v, do, extra, ws, bm)
+
+
+def dkdv_factor(kind, w) -> float:
+    """The dK/dV kernel's FLOPs in units of the forward's F: 2 (S^T, dP^T, dV, dK) where
+    the backward takes the split strategy (dense, d <= 128), 2.5 where that kernel also
+    forms the dQ partials."""
+    return 2.0 if kind == "dense" and w.d != 256 else 2.5
 
 
 def variant_flops(kind, w, bm):
@@ -591,17 +637,55 @@ def run_gpu(args, w, world, rank, local):
     stream = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
 
+    split = d != 256  # the dQ strategy fa_backward takes (decided by measurement; see bwd_strategies)
+
     def step(e=None):
-        # The same four launches fa_backward makes, split so that each kernel is timed.
+        # The same launches fa_backward makes, split so that each kernel is timed.
         if e: e[0].record(stream)
         fa.fa_forward(q, k, v, o, lse, w.causal)
         if e: e[1].record(stream)
-        fa.fa_backward_preprocess(o, do, delta, acc)
+        fa.fa_backward_preprocess(o, do, delta, None if split else acc)
         if e: e[2].record(stream)
-        fa.fa_backward_dkdv(q, k, v, do, lse, delta, acc, dk, dv, w.causal)
+        if split:
+            fa.fa_backward_dk_dv(q, k, v, do, lse, delta, dk, dv, w.causal)
+        else:
+            fa.fa_backward_dkdv(q, k, v, do, lse, delta, acc, dk, dv, w.causal)
         if e: e[3].record(stream)
-        fa.fa_backward_dq_convert(acc, dq)
+        if split:
+            fa.fa_backward_dq(q, k, v, do, lse, delta, dq, w.causal)
+        else:
+            fa.fa_backward_dq_convert(acc, dq)
         if e: e[4].record(stream)
+
+    def backward_strategies(reps=10):
+        """CUDA-event times of the two dQ strategies' backward stages on the
+        resident inputs (the A/B that chose fa_backward's path)."""
+        runs = {"split": [lambda: fa.fa_backward_preprocess(o, do, delta, None),
+                          lambda: fa.fa_backward_dk_dv(q, k, v, do, lse, delta, dk, dv, w.causal),
+                          lambda: fa.fa_backward_dq(q, k, v, do, lse, delta, dq, w.causal)],
+                "accumulated": [lambda: fa.fa_backward_preprocess(o, do, delta, acc),
+                                lambda: fa.fa_backward_dkdv(q, k, v, do, lse, delta, acc, dk, dv, w.causal),
+                                lambda: fa.fa_backward_dq_convert(acc, dq)]}
+        out = {}
+        for name, fns in runs.items():
+            for _ in range(3):
+                for f in fns:
+                    f()
+            tot = [0.0] * 3
+            for _ in range(reps):
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                ev[0].record(stream)
+                for i, f in enumerate(fns):
+                    f()
+                    ev[i + 1].record(stream)
+                torch.cuda.synchronize()
+                for i in range(3):
+                    tot[i] += ev[i].elapsed_time(ev[i + 1])
+            ms = [t / reps for t in tot]
+            out[name] = {"stage_ms": [round(x, 4) for x in ms], "bwd_ms": round(sum(ms), 4),
+                         "bwd_tflops_2p5F": round(2.5 * w.fwd_flops() / (sum(ms) * 1e-3) / 1e12, 1)}
+        fa.fa_device_status()
+        return out
 
     torch.cuda.reset_peak_memory_stats(dev)
     mem_inputs = torch.cuda.memory_allocated(dev)
@@ -707,10 +791,14 @@ def run_gpu(args, w, world, rank, local):
     result = None
     if rank == 0:
         peak = float(peaks["bf16_tflops"])
-        dkdv_tflops = 2.5 * F / (parts[2] * 1e-3) / 1e12
+        # the dK/dV kernel's own work: 4 GEMMs (S^T, dP^T, dV, dK) = 2 F with the split
+        # strategy, 5 (with the dQ partials) = 2.5 F with the accumulated one
+        dkdv_flops = (2.0 if split else 2.5) * F
+        dkdv_tflops = dkdv_flops / (parts[2] * 1e-3) / 1e12
         fwd_tflops = F / (parts[0] * 1e-3) / 1e12
         bwd_ms = parts[1] + parts[2] + parts[3]
         naive_sp = 2 * N * N * 2 * B * H
+        traffic, traffic_src = captured_traffic() if (split and w.name.startswith("C4")) else (None, "no capture")
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -724,15 +812,20 @@ def run_gpu(args, w, world, rank, local):
             "fwdbwd_frac_of_peak": round(value / world / peak, 4),
             "fwdbwd_tflops_3p5F": round(3.5 * F / (ms_step * 1e-3) / 1e12, 1),
             "bwd_tflops_2p5F": round(2.5 * F / (bwd_ms * 1e-3) / 1e12, 1),
-            "kernel_ms": {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
-                          "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)},
-            "roofline": {"bound": "tensor", "kernel": f"fa_bwd_dkdv_kernel<{128 if d == 96 else d},"
-                                                      f"{'causal' if w.causal else 'non-causal'},{w.dtype}>",
+            "kernel_ms": ({"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
+                           "bwd_dk_dv": round(parts[2], 4), "bwd_dq": round(parts[3], 4)} if split else
+                          {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
+                           "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)}),
+            "roofline": {"bound": "tensor",
+                         "kernel": f"{'fa_bwd_dkdv_split_kernel' if split else 'fa_bwd_dkdv_kernel'}"
+                                   f"<{128 if d == 96 else d},{'causal' if w.causal else 'non-causal'},{w.dtype}>",
                          "achieved": round(dkdv_tflops, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(dkdv_tflops / peak, 4),
-                         "traffic": DKDV_TRAFFIC_C4 if w.name.startswith("C4") else None,
+                         "traffic": traffic, "traffic_source": traffic_src,
                          "peak_source": f"{peak_src} bf16_tflops (burst)",
-                         "algorithmic": "10*N^2*d per head (5 GEMMs), halved causal, per launch"},
+                         "algorithmic": ("8*N^2*d per head (4 GEMMs: S^T, dP^T, dV, dK), halved causal, per launch"
+                                         if split else
+                                         "10*N^2*d per head (5 GEMMs), halved causal, per launch")},
             "peak_memory_bytes": int(peak_mem), "inputs_bytes": int(mem_inputs),
             "naive_sp_bytes": int(naive_sp),
             "e2e": {"value": round(world * 2.5 * F / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -746,6 +839,11 @@ def run_gpu(args, w, world, rank, local):
             "clocks": clocks,
         }
     if rank == 0:
+        result["bwd_strategies"] = backward_strategies()
+        result["bwd_strategies"]["note"] = ("dQ by its own kernel (split: preprocess without accumulator, dK/dV, dQ) "
+                                            "vs fp32 dQ partials reduced into an accumulator by the dK/dV kernel "
+                                            "(accumulated: preprocess, dK/dV, convert); the step uses "
+                                            + ("split" if split else "accumulated"))
         from exact_io_aware_forward_gb300.synth import D1
         dms, dbytes, _ = measure_decode(dev, D1, 10, 3)
         dgbs = dbytes / (dms * 1e-3) / 1e9
@@ -762,7 +860,8 @@ def run_gpu(args, w, world, rank, local):
             result[key] = {"workload": vw.name + (f" p={DROP_P}" if kind == "dropout" else ""),
                             "ms": round(sms, 4), "fwdbwd_tflops": round(2.5 * sF / (sms * 1e-3) / 1e12, 1),
                             "fwd_tflops": round(sF / (sparts[0] * 1e-3) / 1e12, 1),
-                            "dkdv_frac_of_peak": round(2.5 * sF / (sparts[2] * 1e-3) / 1e12 / peak, 4)}
+                            "dkdv_frac_of_peak": round(dkdv_factor(kind, vw) * sF / (sparts[2] * 1e-3) / 1e12 / peak,
+                                                       4)}
     if dist:
         dist.destroy_process_group()
     return result
@@ -788,7 +887,7 @@ def measure_long(dev, peak):
             "fwdbwd_frac_of_peak": round(2.5 * F / (ms * 1e-3) / 1e12 / peak, 4),
             "fwd_tflops": round(F / (parts[0] * 1e-3) / 1e12, 1),
             "fwd_frac_of_peak": round(F / (parts[0] * 1e-3) / 1e12 / peak, 4),
-            "dkdv_frac_of_peak": round(2.5 * F / (parts[2] * 1e-3) / 1e12 / peak, 4),
+            "dkdv_frac_of_peak": round(dkdv_factor("dense", w) * F / (parts[2] * 1e-3) / 1e12 / peak, 4),
             "peak_memory_bytes": int(used), "inputs_bytes": int(4 * elem),
             "naive_sp_bytes": int(2 * w.N * w.N * 2 * w.B * w.H),
             "memory": "peak torch allocation of the fwd+bwd steps above the allocations before them: Q, K, V, dO, "

@@ -315,19 +315,16 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     // P^T of this warpgroup's queries: slab (QW h) / 64, from column (QW h) % 64
     uint8_t* ptslab = sPT + ((QW * h) / 64) * C::PT_SLAB;
     const int ptcol = (QW * h) % 64;
-    // -LSE*log2(e) and -D of query column QW h + r (r < QW), fetched one tile ahead
-    float pre_l = 0.f, pre_d = 0.f;
+    // LSE and D of query column QW h + r (r < QW), loaded one tile ahead and
+    // left untouched until they are staged, so the loads' latency is hidden.
+    float pre_l = -pos_inf(), pre_d = 0.f;  // padding query: P = 0
     auto fetch = [&](int i) {
       const int q = i * C::BQ + QW * h + r;
-      if (r < QW) {
-        if (q < N) {
-          const float lq = lse[row0 + q];
-          pre_l = lq == -pos_inf() ? -pos_inf() : -lq * kLog2e;
-          pre_d = -delta[row0 + q];
-        } else {  // padding query: P = 0
-          pre_l = -pos_inf();
-          pre_d = 0.f;
-        }
+      pre_l = -pos_inf();
+      pre_d = 0.f;
+      if (r < QW && q < N) {
+        pre_l = lse[row0 + q];
+        pre_d = delta[row0 + q];
       }
     };
     if (n_it > 0) fetch(i_begin);
@@ -338,8 +335,8 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
       // the staged values of the previous tile have been read by every warp of the warpgroup
       if (it > 0 && !(ok = warp_wait(&ld_empty[h], (it - 1) & 1, abort_flag, status))) break;
       if (r < QW) {
-        sNL[r] = pre_l;
-        sND[r] = pre_d;
+        sNL[r] = pre_l == -pos_inf() ? -pos_inf() : -pre_l * kLog2e;  // a row with no visible key: P = 0
+        sND[r] = -pre_d;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ld_full[h]);

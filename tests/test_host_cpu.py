@@ -108,3 +108,53 @@ def test_varlen_recipe_and_pairs():
     assert q.shape == (8, 2, 64) and k.shape == (11, 2, 64) and do.shape == (8, 2, 64)
     assert cu_q.tolist() == [0, 3, 3, 8] and cu_k.tolist() == [0, 4, 6, 11]
     assert cu_q.dtype == torch.int32
+
+
+def test_roofline_traffic_is_tied_to_the_captured_sources(tmp_path):
+    """The bench reports a captured DRAM traffic only while the kernel's source
+    files hash as they did at capture time."""
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and int(h, 16) >= 0
+    good = tmp_path / "good.md"
+    good.write_text(f"x\ntraffic_bytes_per_launch: 1234\nsource_sha256_16: `{h}`\n")
+    assert bench.captured_traffic(str(good))[0] == 1234
+    stale = tmp_path / "stale.md"
+    stale.write_text("traffic_bytes_per_launch: 1234\nsource_sha256_16: 0000000000000000\n")
+    assert bench.captured_traffic(str(stale)) == (None, "kernel changed since the capture")
+    assert bench.captured_traffic(str(tmp_path / "absent.md"))[0] is None
+
+
+def test_dkdv_flop_factor_follows_the_backward_strategy():
+    assert bench.dkdv_factor("dense", synth.C4) == 2.0
+    assert bench.dkdv_factor("dense", synth.W256) == 2.5
+    assert bench.dkdv_factor("dropout", synth.C4) == 2.5
+
+
+def _exp2_poly_f32(x):
+    """The kernels' FMA-pipe 2^x (exp2_poly2 in fa_ptx.cuh) step by step in
+    float32: clamp, round by adding 1.5 * 2^23, cubic in f, exponent add."""
+    f32 = np.float32
+    x = np.maximum(x.astype(f32), f32(-125.0))
+    t = (x + f32(12582912.0)).astype(f32)
+    n = (t + f32(-12582912.0)).astype(f32)
+    f = (n * f32(-1.0) + x).astype(f32)
+    p = (f * f32(0.0551716685) + f32(0.242611140)).astype(f32)
+    p = (p * f + f32(0.693260968)).astype(f32)
+    p = (p * f + f32(0.999928057)).astype(f32)
+    bits = p.view(np.int32).astype(np.int64) + (t.view(np.int32).astype(np.int64) << 23)
+    return (bits & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+
+
+def test_fma_pipe_exp2_error_bound():
+    """Relative error below 1e-4 (under half an ulp of P rounded to fp16) over
+    the range the softmax uses, exact powers of two at integers, and the
+    clamp below -125."""
+    x = np.concatenate([np.linspace(-125, 20, 400001), -np.logspace(-6, 2, 2001), np.arange(-120, 21)])
+    got = _exp2_poly_f32(x).astype(np.float64)
+    want = np.exp2(np.maximum(x, -125.0))
+    rel = np.abs(got / want - 1)
+    assert rel.max() < 1e-4, rel.max()
+    ints = np.arange(-120, 21).astype(np.float64)
+    assert np.abs(_exp2_poly_f32(ints) / np.exp2(ints) - 1).max() < 1e-4
+    low = _exp2_poly_f32(np.array([-np.inf, -1e30, -200.0]))
+    assert np.all(low > 0) and np.all(low < 3e-38)
