@@ -147,10 +147,16 @@ def backward_head_sampled(q, k, v, do, scale, causal, rows, cols, stripe=2048):
         ds = _softmax_backward(p, a)
         dk += scale * (ds[:, cols].T @ q[r])
         dv += p[:, cols].T @ do[r]
+    return backward_head_rows(q, k, v, do, scale, causal, rows), dk, dv
+
+
+def backward_head_rows(q, k, v, do, scale, causal, rows):
+    """dQ at query rows ``rows`` of one head: row i of dS needs only row i of
+    S, P and A = dO V^T (Tutorial section 3.3), so this costs O(len(rows) N d)."""
+    rows = np.asarray(rows)
     p, _, _ = _softmax_rows(_scores(q, k, scale, causal, rows))
     ds = _softmax_backward(p, do[rows] @ v.T)
-    dq = scale * (ds @ k)
-    return dq, dk, dv
+    return scale * (ds @ k)
 
 
 # --------------------------------------------------------------------------

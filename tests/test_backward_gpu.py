@@ -101,9 +101,43 @@ def test_backward_full_size_sampled(name):
     eo, el = check_forward_heads(q, k, v, o, lse, w.causal, heads=heads, rows=pick)
     assert eo <= O_TOL[w.dtype] and el <= LSE_TOL, (eo, el)
     _check_grads(q, k, v, do, dq, dk, dv, w.causal, heads=heads, rows=pick, cols=pick)
+    # dQ on every head (every L2 head group of every kernel), on a few rows each
+    qf, kf, vf, dof = as_float64(q, k, v, do)
+    s = 1.0 / math.sqrt(w.d)
+    for b in range(w.B):
+        for h in range(w.H):
+            few = np.unique(np.concatenate([[0, 127, 128, w.N - 1], rng.integers(0, w.N, 4)]))
+            ref = A.backward_head_rows(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, w.causal, few)
+            err = rel_fro(dq[b, h].double().numpy()[few], ref)
+            assert err <= GRAD_REL_FRO, (b, h, err)
     # Invariants that hold at any size (P rows sum to 1): sum_j dK_j = 0 and
     # sum_j dV_j = sum_i dO_i, per head, up to the rounding of the inputs.
     dkf = dk.float().sum(dim=2)
     assert float(dkf.abs().max()) <= 1e-2 * float(dk.float().abs().sum(dim=2).max())
     dvs, dos = dv.float().sum(dim=2), do.float().sum(dim=2)
     assert float((dvs - dos).abs().max()) <= 1e-2 * float(dos.abs().max() + 1)
+
+
+def test_backward_several_head_groups_with_a_partial_last_one():
+    """B*H = 40 heads at N = 4096, d = 128: the forward and dQ kernels take
+    heads in L2 groups of 32, the dK/dV kernels in groups of 16, so both see
+    full groups and a partial last group.  Every head is compared on sampled
+    rows (O, LSE, dQ); dK and dV on sampled keys of heads in the first, a
+    middle and the partial last group."""
+    B, H, N, d = 5, 8, 4096, 128
+    q, k, v, do = attention_inputs(B, H, N, d, "bf16", seed=4040)
+    o, lse, dq, dk, dv = gpu_forward_backward(q, k, v, do, True)
+    rng = np.random.default_rng(40)
+    qf, kf, vf, dof = as_float64(q, k, v, do)
+    s = 1.0 / math.sqrt(d)
+    for b in range(B):
+        for h in range(H):
+            few = np.unique(np.concatenate([[0, 127, 128, N - 1], rng.integers(0, N, 4)]))
+            eo, el = check_forward_heads(q, k, v, o, lse, True, heads=[(b, h)], rows=few)
+            assert eo <= O_TOL["bf16"] and el <= LSE_TOL, (b, h, eo, el)
+            ref = A.backward_head_rows(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, True, few)
+            err = rel_fro(dq[b, h].double().numpy()[few], ref)
+            assert err <= GRAD_REL_FRO, (b, h, err)
+    pick = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], rng.integers(0, N, 27)]))
+    heads = [(0, 0), (2, 1), (4, 7)]  # flat heads 0, 17 and 39
+    _check_grads(q, k, v, do, dq, dk, dv, True, heads=heads, rows=pick, cols=pick)

@@ -73,6 +73,9 @@ def test_forward_c3_sampled_heads(name):
 
 @pytest.mark.parametrize("name", ["C4", "C5"])
 def test_forward_full_size_sampled_rows(name):
+    """Every head of the full-size workloads (so every L2 head group and every
+    position inside one), on the tile-edge rows and a few random rows; two
+    heads on 64 rows."""
     w = WORKLOADS[name]
     q, k, v, _ = workload_inputs(w, with_do=False)
     o, lse = gpu_forward(q, k, v, w.causal)
@@ -81,4 +84,9 @@ def test_forward_full_size_sampled_rows(name):
     heads = [(0, 0), (w.B - 1, w.H - 1)]
     eo, el = check_forward_heads(q, k, v, o, lse, w.causal, heads=heads, rows=rows)
     assert eo <= O_TOL[w.dtype] and el <= LSE_TOL, (eo, el)
+    for b in range(w.B):
+        for h in range(w.H):
+            few = np.unique(np.concatenate([[0, 127, 128, w.N - 1], rng.integers(0, w.N, 4)]))
+            eo, el = check_forward_heads(q, k, v, o, lse, w.causal, heads=[(b, h)], rows=few)
+            assert eo <= O_TOL[w.dtype] and el <= LSE_TOL, (b, h, eo, el)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()

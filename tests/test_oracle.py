@@ -215,6 +215,7 @@ def test_sampled_backward_equals_full():
         cols = np.array([0, 5, 128, 298, 299])
         sq, sk, sv = A.backward_head_sampled(q, k, v, do, s, causal, rows, cols, stripe=64)
         assert np.abs(sq - dq[rows]).max() < 1e-13
+        assert np.abs(A.backward_head_rows(q, k, v, do, s, causal, rows[::-1]) - dq[rows[::-1]]).max() < 1e-13
         assert np.abs(sk - dk[cols]).max() < 1e-13
         assert np.abs(sv - dv[cols]).max() < 1e-13
         o, lse = A.forward_head(q, k, v, s, causal)
