@@ -247,10 +247,14 @@ def measure_decode(dev, w, steps, warmup):
 
 
 def run_decode(args, world, rank, local):
+    import dataclasses
+
     import torch
 
     import exact_io_aware_forward_gb300 as fa
     from exact_io_aware_forward_gb300.synth import D1 as w
+    if args.nq != w.Nq:
+        w = dataclasses.replace(w, Nq=args.nq, name=f"D1 decode causal Nq={args.nq} Nk={w.Nk} d={w.d} {w.dtype}")
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -845,10 +849,13 @@ def run_gpu(args, w, world, rank, local):
                                             "(accumulated: preprocess, dK/dV, convert); the step uses "
                                             + ("split" if split else "accumulated"))
         from exact_io_aware_forward_gb300.synth import D1
-        dms, dbytes, _ = measure_decode(dev, D1, 10, 3)
-        dgbs = dbytes / (dms * 1e-3) / 1e9
-        result["decode"] = {"workload": D1.name, "ms": round(dms, 4), "GB_per_s": round(dgbs, 1),
-                            "frac_of_hbm_peak": round(dgbs / float(peaks["hbm_gbs"]), 4)}
+        import dataclasses
+        for key, dw in (("decode", D1), ("decode_nq16", dataclasses.replace(D1, Nq=16, name="D1 Nq=16")),
+                        ("decode_nq64", dataclasses.replace(D1, Nq=64, name="D1 Nq=64"))):
+            dms, dbytes, _ = measure_decode(dev, dw, 10, 3)
+            dgbs = dbytes / (dms * 1e-3) / 1e9
+            result[key] = {"workload": dw.name, "ms": round(dms, 4), "GB_per_s": round(dgbs, 1),
+                           "frac_of_hbm_peak": round(dgbs / float(peaks["hbm_gbs"]), 4)}
         from exact_io_aware_forward_gb300.synth import S1
         from exact_io_aware_forward_gb300.synth import V1
         from exact_io_aware_forward_gb300.synth import W96, W256
@@ -933,6 +940,7 @@ def main():
                          "training workload with dropout p=0.1; varlen: fwd+bwd of a packed batch of "
                          "16 causal sequences")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing (rank 0, N=1)")
+    ap.add_argument("--nq", type=int, default=1, help="--mode decode: queries per head (1: the D1 workload)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

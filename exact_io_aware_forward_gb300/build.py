@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_dropout.cu", "fa_fwd_varlen.cu", "fa_fwd256.cu", "fa_bwd.cu",
            "fa_bwd_dropout.cu",
            "fa_bwd_varlen.cu", "fa_bwd_aux.cu", "fa_bwd_split.cu",
-           "fa_bwd_noalloc.cu", "fa_decode.cu"]
+           "fa_bwd_noalloc.cu", "fa_decode.cu", "fa_decode_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]

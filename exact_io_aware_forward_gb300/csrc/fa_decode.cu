@@ -1,4 +1,6 @@
-// Split-KV forward for few queries against many keys (decoding).
+// Split-KV forward for few queries against many keys (decoding) on the CUDA
+// cores, used at d = 256 (d <= 128 runs the tensor-core kernel of
+// fa_decode_tc.cu, which shares this file's workspace layout and combine).
 //
 // The key range of every head is cut into `num_splits` contiguous chunks; a
 // CTA evaluates exact attention of up to QG queries over one chunk with the
@@ -292,14 +294,19 @@ cudaError_t launch_split_q(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 template <int D, bool BF16>
-cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  cudaError_t e = a.causal ? launch_split_q<D, BF16, true>(a, stream) : launch_split_q<D, BF16, false>(a, stream);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_combine_t(const DecodeArgs& a, cudaStream_t stream) {
   const long long rows = (long long)a.BH * a.Nq;
   if (rows > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fa_decode_combine_kernel<D, BF16><<<(unsigned)rows, D / 2, 0, stream>>>(
       a.o_part, a.lse_part, static_cast<uint32_t*>(a.o), a.lse, (int)rows, a.num_splits);
   return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+  cudaError_t e = a.causal ? launch_split_q<D, BF16, true>(a, stream) : launch_split_q<D, BF16, false>(a, stream);
+  if (e != cudaSuccess) return e;
+  return launch_combine_t<D, BF16>(a, stream);
 }
 
 }  // namespace
@@ -315,9 +322,29 @@ int decode_default_splits(int BH, int Nq, int Nk) {
   return s < 1 ? 1 : (int)s;
 }
 
+int decode_tc_default_splits(int BH, int Nq, int Nk) {
+  // one CTA per SM (shared memory): about four waves of CTAs, at least eight
+  // 128-key tiles per chunk
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long tiles = (long long)BH * ((Nq + 127) / 128);
+  const long long want = (4LL * sms + tiles - 1) / tiles;
+  const long long max_splits = (Nk + 1023) / 1024;
+  long long s = want < max_splits ? want : max_splits;
+  if (s > 1024) s = 1024;
+  return s < 1 ? 1 : (int)s;
+}
+
 int decode_chunk(int Nk, int num_splits) {
   const int per = (Nk + num_splits - 1) / num_splits;
   return ((per + kTK - 1) / kTK) * kTK;
+}
+
+cudaError_t launch_decode_combine(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream) {
+  if (d == 64) return bf16 ? launch_combine_t<64, true>(a, stream) : launch_combine_t<64, false>(a, stream);
+  if (d == 128) return bf16 ? launch_combine_t<128, true>(a, stream) : launch_combine_t<128, false>(a, stream);
+  if (d == 256) return bf16 ? launch_combine_t<256, true>(a, stream) : launch_combine_t<256, false>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream) {

@@ -42,6 +42,10 @@ CASES = [
     (1, 2, 3, 1000, 64, "bf16", True, 7), (1, 2, 4, 1000, 128, "fp16", False, 3), (2, 2, 5, 4100, 128, "bf16", True, 0),
     (1, 3, 16, 700, 64, "fp16", True, 1), (1, 2, 17, 2000, 128, "bf16", True, 9), (1, 1, 40, 40, 128, "bf16", True, 0),
     (2, 2, 40, 5000, 64, "bf16", False, 0), (1, 2, 8, 257, 128, "fp16", True, 64),
+    # 8 queries or more at d <= 128: the tensor-core split kernel (128-query tiles)
+    (1, 2, 64, 3333, 128, "bf16", True, 0), (1, 2, 128, 1000, 64, "fp16", False, 0),
+    (1, 1, 129, 4097, 128, "bf16", True, 0), (2, 1, 200, 1500, 128, "fp16", True, 3),
+    (1, 2, 9, 130, 64, "bf16", False, 0), (1, 2, 100, 100, 128, "bf16", True, 1),
     # head dimension 256
     (1, 2, 1, 3000, 256, "bf16", True, 0), (1, 2, 4, 999, 256, "fp16", False, 5), (1, 1, 20, 700, 256, "bf16", True, 0),
 ]
@@ -78,4 +82,20 @@ def test_decode_full_size_sampled_heads():
     o, lse = fa.forward_decode(q.to(dev), k.to(dev), v.to(dev), causal=True)
     fa.fa_device_status()
     eo, el = _check(q, k, v, o.cpu(), lse.cpu(), True, heads=[(0, 0), (1, 17), (3, 31)])
+    assert eo <= O_TOL["bf16"] and el <= LSE_TOL, (eo, el)
+
+
+@pytest.mark.parametrize("nq", [16, 64])
+def test_decode_full_size_several_queries(nq):
+    """The D1 shape (B=4, H=32, Nk=32768, d=128, bf16, causal) with 16 and 64
+    queries per head (the tensor-core split kernel), on sampled heads."""
+    import dataclasses
+
+    from exact_io_aware_forward_gb300.synth import D1, decode_inputs
+    w = dataclasses.replace(D1, Nq=nq, name=f"D1 Nq={nq}")
+    q, k, v = decode_inputs(w)
+    dev = torch.device("cuda:0")
+    o, lse = fa.forward_decode(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    fa.fa_device_status()
+    eo, el = _check(q, k, v, o.cpu(), lse.cpu(), True, heads=[(0, 0), (2, 9), (3, 31)])
     assert eo <= O_TOL["bf16"] and el <= LSE_TOL, (eo, el)
