@@ -670,6 +670,8 @@ def run_gpu(args, w, world, rank, local):
                 "accumulated": [lambda: fa.fa_backward_preprocess(o, do, delta, acc),
                                 lambda: fa.fa_backward_dkdv(q, k, v, do, lse, delta, acc, dk, dv, w.causal),
                                 lambda: fa.fa_backward_dq_convert(acc, dq)]}
+        if not split:  # d = 256: the split stages do not exist
+            runs.pop("split")
         out = {}
         for name, fns in runs.items():
             for _ in range(3):
