@@ -24,7 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_dropout.cu", "fa_fwd_varlen.cu", "fa_fwd256.cu", "fa_bwd.cu",
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_persist.cu", "fa_fwd_dropout.cu", "fa_fwd_varlen.cu", "fa_fwd256.cu", "fa_bwd.cu",
            "fa_bwd_dropout.cu",
            "fa_bwd_varlen.cu", "fa_bwd_aux.cu", "fa_bwd_split.cu",
            "fa_bwd_noalloc.cu", "fa_decode.cu", "fa_decode_tc.cu"]

@@ -1,5 +1,7 @@
-// Forward pass: launch dispatch for the dense and block-sparse instances of
-// the kernel in fa_fwd_kernel.cuh.
+// Forward pass: launch dispatch for dense layouts without dropout.  Block
+// masks run the kernel in fa_fwd_kernel.cuh; plain dense attention runs the
+// kernel of fa_fwd_persist.cu (Q with a producer of its own, per-query-tile
+// O hand-off, persistent CTAs at d = 64).
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -8,7 +10,7 @@ namespace {
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_fwd_s(const FwdArgs& a, cudaStream_t stream) {
   return a.block_mask ? launch_fwd_t<D, CAUSAL, BF16, true, false, false>(a, stream)
-                      : launch_fwd_t<D, CAUSAL, BF16, false, false, false>(a, stream);
+                      : launch_forward_persistent(D, CAUSAL, BF16, a, stream);
 }
 
 }  // namespace

@@ -1,7 +1,8 @@
 // Forward pass of exact attention on sm_103a: the kernel template, shared by
-// the translation units that instantiate it (fa_fwd.cu: dense and
-// block-sparse; fa_fwd_dropout.cu: dropout; fa_fwd_varlen.cu: packed
-// variable-length batches; fa_fwd256.cu reuses its helpers for d = 256).
+// the translation units that instantiate it (fa_fwd.cu: block-sparse;
+// fa_fwd_dropout.cu: dropout; fa_fwd_varlen.cu: packed variable-length
+// batches), and the helpers that fa_fwd_persist.cu (plain dense attention)
+// and fa_fwd256.cu (d = 256) reuse.
 //
 // Algorithm: the online-softmax recurrence of "FlashAttention 为什么不需要存下
 // 注意力矩阵" (jefxiong.cn), section 3.2 -- per query row a reference max m, a
@@ -80,8 +81,8 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = QT * TILE;
   static constexpr int OFF_BAR = OFF_RING + NS * TILE;
-  // q_full, ring_full[NS], ring_empty[NS], s_full[2], p_full[2], o_full, drain
-  static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1;
+  // q_full, ring_full[NS], ring_empty[NS], s_full[2], p_full[2], o_full[2], drain[2]
+  static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
   static constexpr int THREADS = 384;
@@ -129,6 +130,123 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// One key tile of the online softmax for the calling thread's query row
+// (one TMEM lane): reads the tile's 128 scores (columns tS ..), masks keys
+// >= Nk and, when CAUSAL, keys > row_off (the tile's first row sees keys up
+// to tile_off); moves the reference max m_ref when the tile's max exceeds it
+// by more than kRescaleThreshold, scaling l, l_mma and, if `o_live` (earlier
+// tiles of this row are in O), the O row in TMEM (columns tO ..); writes P
+// as packed 16-bit pairs over the scores, with dropped entries zeroed when
+// DROP.  sum2 / sumr2 return the tile's sum of P as computed and as rounded
+// to 16 bit (pairs of partial sums), for the caller to add into l / l_mma
+// after it has handed P to the tensor core.  The TMEM stores are not yet
+// waited for.
+template <int D, bool CAUSAL, bool BF16, bool DROP>
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int kbase, int Nk, int row_off,
+                                             int tile_off, float scale_log2, bool o_live,
+                                             const uint32_t (&keep)[4], float& m_ref, float& l, float& l_mma,
+                                             uint64_t& sum2, uint64_t& sumr2) {
+  constexpr int kBN = 128;
+  float s[4][32];
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, s[cc]);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(s[cc]);
+
+  const bool need_mask = (kbase + kBN > Nk) || (CAUSAL && kbase + kBN - 1 > tile_off);
+  if (need_mask) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int key = kbase + 32 * cc + i;
+        if (key >= Nk || (CAUSAL && key > row_off)) s[cc][i] = neg_inf();
+      }
+  }
+  float mx = s[0][0];
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) mx = max3(mx, s[cc][i], s[cc][i + 1]);
+  const float m_new = fmaxf(m_ref, mx * scale_log2);
+  float corr = 1.f;
+  bool rescale_o = false;
+  if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold)) {
+    const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
+    corr = ex2_approx(m_ref - m_use);
+    l *= corr;
+    l_mma *= corr;
+    rescale_o = o_live;
+    m_ref = m_use;
+  }
+  const float neg_m = (m_ref == neg_inf()) ? 0.f : -m_ref;
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+  const uint64_t nm2 = f2_pack(neg_m, neg_m);
+  sum2 = f2_pack(0.f, 0.f);
+  sumr2 = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {  // 32 scores -> 16 packed pairs -> 16 TMEM columns
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(s[cc][2 * i], s[cc][2 * i + 1]), sc2, nm2), x0, x1);
+      const float p0 = ex2_approx(x0);
+      const float p1 = ex2_approx(x1);
+      sum2 = f2_add(sum2, f2_pack(p0, p1));
+      pk[i] = pack2(p0, p1, BF16);
+      float r0, r1;
+      unpack2(pk[i], BF16, r0, r1);
+      sumr2 = f2_add(sumr2, f2_pack(r0, r1));
+    }
+    if (DROP) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] &= pair_keep_mask(keep[cc], i);
+    }
+    tmem_st16(tS + 16 * cc, pk);
+  }
+  if (rescale_o) {
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      float o[32];
+      tmem_ld32(tO + 32 * cc, o);
+      tmem_ld_wait(o);
+      const uint64_t corr2 = f2_pack(corr, corr);
+      uint32_t ou[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float a, b;
+        f2_unpack(f2_mul(f2_pack(o[i], o[i + 1]), corr2), a, b);
+        ou[i] = __float_as_uint(a);
+        ou[i + 1] = __float_as_uint(b);
+      }
+      tmem_st32(tO + 32 * cc, ou);
+    }
+  }
+}
+
+// Epilogue of one query row: reads the row's O accumulator (columns tO ..),
+// multiplies it by inv_l and, if `in_range`, writes the first dh features
+// as 16-bit values to `orow` (dh / 8 16-byte chunks, contiguous in memory;
+// features past dh, zero-padded inputs, are not stored).
+template <int D, bool BF16>
+__device__ __forceinline__ void store_o_row(uint32_t tO, uint4* orow, int dh, float inv_l, bool in_range) {
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    if (32 * cc >= dh) break;
+    float ov[32];
+    tmem_ld32(tO + 32 * cc, ov);
+    tmem_ld_wait(ov);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, BF16);
+    if (in_range) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) orow[4 * cc + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+}
+
 template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -149,7 +267,7 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* s_full = ring_empty + C::NS;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_full = p_full + 2;
-  uint64_t* drain = o_full + 1;
+  uint64_t* drain = o_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -200,8 +318,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);
     }
-    mbar_init(o_full, 1);
-    mbar_init(drain, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&o_full[t], 1);
+      mbar_init(&drain[t], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -277,29 +397,36 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t kIdPV = idesc_f16(128, D, BF16, false, true);
       const uint32_t sq = smem_u32(sQ);
       const uint32_t sring = smem_u32(sRing);
+      // descriptors of the first Q tile and of ring slot 0 (K: K-major; V: MN-major)
+      const uint64_t dq0 = sdesc_sw128(sq, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sring, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sring, C::SLAB, 1024);
       auto issue_s = [&](int t, int j) {
-        const uint32_t a0 = sq + t * C::TILE;
-        const uint32_t b0 = sring + kslot(j) * C::TILE;
+        const uint64_t da = sdesc_advance(dq0, t * C::TILE);
+        const uint64_t db = sdesc_advance(dk0, kslot(j) * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::SLAB + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S + t * C::BN, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
-                 kIdS, kk > 0);
+          mma_ss(tmem + C::COL_S + t * C::BN, sdesc_advance(da, off), sdesc_advance(db, off), kIdS, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int j, bool first) {
-        const uint32_t b0 = sring + vslot(j) * C::TILE;
+        const uint64_t dv = sdesc_advance(dv0, vslot(j) * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk) {
           mma_ts(tmem + C::COL_O + t * D, tmem + C::COL_S + t * C::BN + kk * 8,
-                 sdesc_sw128(b0 + kk * 2048, C::SLAB, 1024), kIdPV, (!first || kk > 0));
+                 sdesc_advance(dv, kk * 2048), kIdPV, (!first || kk > 0));
         }
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusTimeout);
       if constexpr (!SPARSE) {
         // Per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j).  PV_t(j-1) is
         // issued before S_t(j), whose columns hold P_t(j-1), by the same
-        // thread (in-order).
+        // thread (in-order).  One thread issues both query tiles' products:
+        // that order makes the tensor core alternate between the tiles while
+        // each tile's softmax runs (two issuers, one per tile, measured
+        // slower: 1.065 against 0.903 ms on the causal N = 8192, d = 128
+        // forward).
         for (int j = 0; ok && j < n1; ++j) {
           if (!(ok = mbar_wait(&ring_full[kslot(j)], kpar(j), abort_flag, status, kStatusTimeout))) break;
           if (j >= 1 && !(ok = mbar_wait(&ring_full[vslot(j - 1)], vpar(j - 1), abort_flag, status, kStatusTimeout)))
@@ -309,6 +436,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = mbar_wait(&p_full[0], (j - 1) & 1, abort_flag, status, kStatusTimeout))) break;
             tc_fence_after();
             issue_pv(0, j - 1, j == 1);
+            if (j == n0) mma_commit(&o_full[0]);  // query tile 0's last product (causal)
           }
           if (j < n0) {
             issue_s(0, j);
@@ -339,10 +467,18 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) issue_pv(1, jl, jl == 0);
           }
         }
+        if (ok) {
+          if (n0 == n1 || n0 == 0) mma_commit(&o_full[0]);
+          mma_commit(&o_full[1]);
+        }
         // Both query tiles run every key tile they see, query tile 1 also when
         // it starts past the last row (an odd number of query tiles): its
         // scores are computed and its rows never stored.
         if (ok) count_score_blocks(status, kCountForward, 4ull * (unsigned)(n0 + n1));
+        if (!ok) {  // every MMA issued so far must finish before TMEM is freed
+          mma_commit(&drain[0]);
+          drain_wait(&drain[0], 0);
+        }
       } else {
         // Per load-order position u: PV_0(prev), S_0(u), PV_1(prev), S_1(u), where
         // prev is the previous position; a query tile skips the products of the
@@ -399,11 +535,14 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         if (ok) count_score_blocks(status, kCountForward, 4ull * (unsigned)(c0 + c1));
-      }
-      if (ok) mma_commit(o_full);
-      if (!ok) {  // every MMA issued so far must finish before TMEM is freed
-        mma_commit(drain);
-        drain_wait(drain, 0);
+        if (ok) {
+          mma_commit(&o_full[0]);
+          mma_commit(&o_full[1]);
+        }
+        if (!ok) {  // every MMA issued so far must finish before TMEM is freed
+          mma_commit(&drain[0]);
+          drain_wait(&drain[0], 0);
+        }
       }
     }
   } else if (warp >= 4) {
@@ -437,83 +576,9 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!(ok = warp_wait(&s_full[t], c & 1, abort_flag, status))) break;
       tc_fence_after();
-      float s[4][32];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, s[cc]);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(s[cc]);
-
-      const int kbase = j * C::BN;
-      const bool need_mask = (kbase + C::BN > Nk) || (CAUSAL && kbase + C::BN - 1 > tile_off);
-      if (need_mask) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int key = kbase + 32 * cc + i;
-            if (key >= Nk || (CAUSAL && key > row_off)) s[cc][i] = neg_inf();
-          }
-      }
-      float mx = s[0][0];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) mx = max3(mx, s[cc][i], s[cc][i + 1]);
-      const float m_new = fmaxf(m_ref, mx * scale_log2);
-      float corr = 1.f;
-      bool rescale_o = false;
-      if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold)) {
-        const float m_use = (m_new == neg_inf()) ? 0.f : m_new;
-        corr = ex2_approx(m_ref - m_use);
-        l *= corr;
-        l_mma *= corr;
-        rescale_o = c > 0;
-        m_ref = m_use;
-      }
-      const float neg_m = (m_ref == neg_inf()) ? 0.f : -m_ref;
-      const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
-      const uint64_t nm2 = f2_pack(neg_m, neg_m);
-      uint64_t sum2 = f2_pack(0.f, 0.f);   // sum of P as computed (fp32)
-      uint64_t sumr2 = f2_pack(0.f, 0.f);  // sum of P as rounded for the MMA
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {  // 32 scores -> 16 packed pairs -> 16 TMEM columns
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[cc][2 * i], s[cc][2 * i + 1]), sc2, nm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          sum2 = f2_add(sum2, f2_pack(p0, p1));
-          pk[i] = pack2(p0, p1, BF16);
-          float r0, r1;
-          unpack2(pk[i], BF16, r0, r1);
-          sumr2 = f2_add(sumr2, f2_pack(r0, r1));
-        }
-        if (DROP) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] &= pair_keep_mask(keep[cc], i);
-        }
-        tmem_st16(tS + 16 * cc, pk);
-      }
-      if (rescale_o) {
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float o[32];
-          tmem_ld32(tO + 32 * cc, o);
-          tmem_ld_wait(o);
-          const uint64_t corr2 = f2_pack(corr, corr);
-          uint32_t ou[32];
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float a, b;
-            f2_unpack(f2_mul(f2_pack(o[i], o[i + 1]), corr2), a, b);
-            ou[i] = __float_as_uint(a);
-            ou[i + 1] = __float_as_uint(b);
-          }
-          tmem_st32(tO + 32 * cc, ou);
-        }
-      }
+      uint64_t sum2, sumr2;  // this tile's sum of P as computed (fp32) and as rounded for the MMA
+      softmax_tile<D, CAUSAL, BF16, DROP>(tS, tO, j * C::BN, Nk, row_off, tile_off, scale_log2, c > 0, keep, m_ref,
+                                          l, l_mma, sum2, sumr2);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -533,7 +598,7 @@ __global__ void __launch_bounds__(384, 1)
     // faster with per-row stores, and packed layouts need them (a tile's
     // last rows can belong to the next sequence).
     constexpr bool kStageO = !VARLEN && (SPARSE || DROP);
-    if (ok) ok = warp_wait(o_full, 0, abort_flag, status);
+    if (ok) ok = warp_wait(&o_full[t], 0, abort_flag, status);
     const long long frow = sv.qflat(row);
     const bool has_o = ok && c > 0;
     if (ok && c == 0) {  // no key tile for this query tile: empty softmax, O = 0, LSE = -inf
@@ -571,22 +636,7 @@ __global__ void __launch_bounds__(384, 1)
                 make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       } else {
-        // Each thread writes its own row: dh/8 16-byte chunks, contiguous in memory.
-        uint4* orow = reinterpret_cast<uint4*>(o) + frow * (dh / 8);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          if (32 * cc >= dh) break;  // features past dh (zero-padded inputs) are not stored
-          float ov[32];
-          tmem_ld32(tO + 32 * cc, ov);
-          tmem_ld_wait(ov);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l, BF16);
-          if (row < Nq) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) orow[4 * cc + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
-        }
+        store_o_row<D, BF16>(tO, reinterpret_cast<uint4*>(o) + frow * (dh / 8), dh, inv_l, row < Nq);
       }
       if (row < Nq) {
         const float m_fin = (m_ref == neg_inf()) ? 0.f : m_ref;

@@ -69,6 +69,9 @@ struct FwdArgs {
   unsigned int* status;                // device status word
 };
 cudaError_t launch_forward(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
+// Dense layouts without block mask or dropout: the persistent kernel (a CTA
+// takes further work items from CTAs of its grid that have not started).
+cudaError_t launch_forward_persistent(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_forward_dropout(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 // Packed variable-length instances (a.lay.cu_q != nullptr), with or without dropout.
 cudaError_t launch_forward_varlen(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);

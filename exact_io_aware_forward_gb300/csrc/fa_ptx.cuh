@@ -106,6 +106,43 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Pulls a tile into L2 ahead of its tma_load_3d (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Asks the hardware to cancel the launch of a CTA of this grid that has not
+// started yet, so that the caller can do its work instead.  The 16-byte
+// answer is written to `resp` (16-byte aligned shared memory) and completes
+// 16 bytes of transaction on `bar`.  After an answer that reports no
+// cancellation, no further request may be made by this CTA.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+          smem_u32(resp)),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+// Reads an answer that has landed: true if a CTA was cancelled, with its
+// blockIdx.x in *cta_x.
+__device__ __forceinline__ bool clc_cancelled(const void* resp, int* cta_x) {
+  const __int128 v = *reinterpret_cast<const volatile __int128*>(resp);
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, %1;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "q"(v));
+  if (ok) asm volatile("clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, %1;" : "=r"(x) : "q"(v));
+  *cta_x = static_cast<int>(x);
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -164,6 +201,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// The descriptor of the address `bytes` further on: only the start-address
+// field moves (shared-memory addresses stay below 256 KB, so the field's 14
+// bits do not carry into the leading-byte-offset field).
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(desc));
+  lo += bytes >> 4;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
 }
 
 // Instruction descriptor, kind::f16 with fp32 accumulation.
