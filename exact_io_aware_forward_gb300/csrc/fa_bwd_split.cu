@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
         const uint64_t db = sdesc_sw128(aQD + qs * C::TILE, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = ((kk >> 2) * C::SLAB + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + col_t, da + o, db + o, kIdT, kk > 0);
+          const uint32_t o = (kk >> 2) * C::SLAB + (kk & 3) * 32;
+          mma_ss(tmem + col_t, sdesc_advance(da, o), sdesc_advance(db, o), kIdT, kk > 0);
         }
       };
       auto issue_dv = [&](int qs, bool first) {  // dV += P^T dO, P^T from shared memory
@@ -238,8 +238,8 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
         const uint64_t db = sdesc_sw128(aB2 + qs * C::TILE, C::SLAB, 1024);
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk) {
-          const uint32_t oa = ((kk >> 2) * C::PT_SLAB + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_DV, da + oa, db + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
+          const uint32_t oa = (kk >> 2) * C::PT_SLAB + (kk & 3) * 32;
+          mma_ss(tmem + C::COL_DV, sdesc_advance(da, oa), sdesc_advance(db, kk * 2048), kIdAcc, !(first && kk == 0));
         }
       };
       auto issue_dk = [&](int qs, bool first) {  // dK += dS^T Q, dS^T from TMEM
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
           // query columns 16kk .. 16kk+15: warpgroup kk/2 wrote them as 16-bit
           // pairs from its first column, 8 columns per 16 queries
           const uint32_t a = tmem + C::COL_DP + 32 * (kk >> 1) + 8 * (kk & 1);
-          mma_ts(tmem + C::COL_DK, a, db + ((kk * 2048) >> 4), kIdAcc, !(first && kk == 0));
+          mma_ts(tmem + C::COL_DK, a, sdesc_advance(db, kk * 2048), kIdAcc, !(first && kk == 0));
         }
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag, status, kStatusTimeout);
@@ -621,8 +621,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           const uint64_t db = sdesc_sw128(aK + (jt % C::NK) * C::TILE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t o = ((kk >> 2) * C::SLAB + (kk & 3) * 32) >> 4;
-            mma_ts(tmem + C::COL_S, tmem + C::COL_QA + 8 * kk, db + o, kIdT, kk > 0);
+            const uint32_t o = (kk >> 2) * C::SLAB + (kk & 3) * 32;
+            mma_ts(tmem + C::COL_S, tmem + C::COL_QA + 8 * kk, sdesc_advance(db, o), kIdT, kk > 0);
           }
           mma_commit(s_full);
         }
@@ -636,8 +636,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           const uint64_t db = sdesc_sw128(aV + (jt % C::NV) * C::TILE, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t o = ((kk >> 2) * C::SLAB + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::COL_DP, da + o, db + o, kIdT, kk > 0);
+            const uint32_t o = (kk >> 2) * C::SLAB + (kk & 3) * 32;
+            mma_ss(tmem + C::COL_DP, sdesc_advance(da, o), sdesc_advance(db, o), kIdT, kk > 0);
           }
           mma_commit(dp_full);
           mma_commit(&v_empty[jt % C::NV]);
@@ -649,7 +649,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           const uint64_t db = sdesc_sw128(aK + (jt % C::NK) * C::TILE, C::SLAB, 1024);
 #pragma unroll
           for (int kk = 0; kk < C::BKV / 16; ++kk)
-            mma_ts(tmem + C::COL_DQ, tmem + C::COL_DS + 8 * kk, db + ((kk * 2048) >> 4), kIdDq, !(jt == 0 && kk == 0));
+            mma_ts(tmem + C::COL_DQ, tmem + C::COL_DS + 8 * kk, sdesc_advance(db, kk * 2048), kIdDq,
+                   !(jt == 0 && kk == 0));
           mma_commit(ds_empty);
           mma_commit(&k_empty[jt % C::NK]);  // K_j: S(j) finished before dS(j) existed
         }

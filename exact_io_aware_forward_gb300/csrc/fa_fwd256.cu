@@ -183,25 +183,28 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t kIdPV = idesc_f16(128, D, BF16, false, true);      // B (V) MN-major
       const uint32_t sq = smem_u32(sQ);
       const uint32_t sring = smem_u32(sRing);
+      // descriptors of Q and of ring slot 0 (K: K-major; V: MN-major), advanced per K-step
+      const uint64_t dq = sdesc_sw128(sq, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sring, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sring, C::KV_SLAB, 1024);
       int pos = 0;  // next ring position to consume
       // S(j) = Q K(j)^T into S buffer b: 16 k-steps of 16 features.
       auto issue_s = [&](int b, int slot) {
-        const uint32_t kb = sring + slot * C::KV_TILE;
+        const uint64_t dk = sdesc_advance(dk0, slot * C::KV_TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::Q_SLAB + (kk & 3) * 32;
           const uint32_t ob = (kk >> 2) * C::KV_SLAB + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S + 64 * b, sdesc_sw128(sq + oa, 16, 1024), sdesc_sw128(kb + ob, 16, 1024), kIdS,
-                 kk > 0);
+          mma_ss(tmem + C::COL_S + 64 * b, sdesc_advance(dq, oa), sdesc_advance(dk, ob), kIdS, kk > 0);
         }
       };
       // O += P(j) V(j): P read from S buffer b (16-bit pairs, 8 columns per 16 keys).
       auto issue_pv = [&](int b, int slot, bool first) {
-        const uint32_t vb = sring + slot * C::KV_TILE;
+        const uint64_t dv = sdesc_advance(dv0, slot * C::KV_TILE);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + C::COL_O, tmem + C::COL_S + 64 * b + kk * 8, sdesc_sw128(vb + kk * 2048, C::KV_SLAB, 1024),
-                 kIdPV, !first || kk > 0);
+          mma_ts(tmem + C::COL_O, tmem + C::COL_S + 64 * b + kk * 8, sdesc_advance(dv, kk * 2048), kIdPV,
+                 !first || kk > 0);
       };
       auto take = [&](bool& ok) {  // wait for the next ring position; returns its slot
         const int slot = pos % C::NS;
