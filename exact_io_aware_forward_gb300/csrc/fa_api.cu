@@ -174,10 +174,9 @@ fa_status run_forward(const Shape& s, const void* q, const void* k, const void* 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
   if (s.d == 256 && block_mask) return FA_ERR_UNSUPPORTED;
-  const int kv_rows = s.d == 256 ? 64 : 128;  // the d = 256 kernel streams 64-key tiles
   fa::FwdArgs a;
-  if (!make_map(&a.tm_q, q, s, false, 128) || !make_map(&a.tm_k, k, s, true, kv_rows) ||
-      !make_map(&a.tm_v, v, s, true, kv_rows) || !make_map(&a.tm_o, o, s, false, 128))
+  if (!make_map(&a.tm_q, q, s, false, 128) || !make_map(&a.tm_k, k, s, true, 128) ||
+      !make_map(&a.tm_v, v, s, true, 128) || !make_map(&a.tm_o, o, s, false, 128))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;

@@ -9,16 +9,20 @@
 // d <= 128 kernel (2 x S + 2 x O = 768 columns) do not fit.  Here a CTA owns
 // ONE 128-row query tile and overlaps its own softmax with the tensor core by
 // double-buffering S:
-//   TMEM  S_a (64 cols) | S_b (64 cols) | O (256 cols)
+//   TMEM  S_a (128 cols) | S_b (128 cols) | O (256 cols)
 //   MMA order  S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ...
 // so the tensor core computes PV(j) and S(j+2) while the softmax warps work on
-// S(j+1).  Key tiles are 64 keys (the S products are 128 x 64 x 256) so that
-// Q (64 KB) and a ring of four 32 KB K / V tiles fit in shared memory, which
-// keeps K(j+2) and V(j+1) in flight while PV(j) runs.
+// S(j+1).  Key tiles are 128 keys, so every product is a 128 x 128 x 16
+// instruction: S over 16 K-steps of the 256 features, and PV as two N = 128
+// products, one per 128-feature half of V and O (64-key tiles, which made
+// the S products N = 64, cost nearly as much per instruction for half the
+// work).  K and V move through the ring in 128-feature halves (32 KB slots),
+// so that Q (64 KB) and five slots fit in shared memory.
 //
 // Roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer: Q once, then K / V tiles in consumption order
-//               K0 K1 V0 K2 V1 K3 V2 ... through a 4-slot ring.
+//   warp 0      TMA producer: Q once, then K / V half tiles in consumption
+//               order K0 K1 V0 K2 V1 K3 V2 ... (each as its two feature
+//               halves) through a 5-slot ring.
 //   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma.
 //   warps 2-5   softmax, one query row per thread (TMEM lane), then the
 //               epilogue (O / l_mma, LSE).
@@ -32,13 +36,13 @@ namespace {
 struct Fwd256Cfg {
   static constexpr int D = 256;
   static constexpr int BM = 128;                   // query rows per CTA
-  static constexpr int BN = 64;                    // keys per tile
+  static constexpr int BN = 128;                   // keys per tile
   static constexpr int Q_SLAB = 128 * 64 * 2;      // 128 rows x 64 features x 16 bit
-  static constexpr int KV_SLAB = 64 * 64 * 2;      // 64 rows x 64 features
+  static constexpr int KV_SLAB = 128 * 64 * 2;     // 128 keys x 64 features
   static constexpr int SLABS = D / 64;
   static constexpr int Q_TILE = SLABS * Q_SLAB;    // 64 KB
-  static constexpr int KV_TILE = SLABS * KV_SLAB;  // 32 KB
-  static constexpr int NS = 4;                     // ring slots
+  static constexpr int KV_TILE = 2 * KV_SLAB;      // one ring slot: 128 keys x 128 features, 32 KB
+  static constexpr int NS = 5;                     // ring slots
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = Q_TILE;
   static constexpr int OFF_BAR = OFF_RING + NS * KV_TILE;
@@ -48,13 +52,15 @@ struct Fwd256Cfg {
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr int THREADS = 192;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0;    // S_a at 0, S_b at 64
-  static constexpr uint32_t COL_O = 128;  // 256 columns
+  static constexpr uint32_t COL_S = 0;    // S_a at 0, S_b at 128
+  static constexpr uint32_t COL_O = 256;  // 256 columns
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 // The ring carries K and V tiles in the order the MMA thread consumes them:
-// K0, K1, then V(j), K(j+2) for j = 0, 1, ... (K(j+2) only while it exists).
-// Position p of that sequence -> (is_v, tile).
+// K0, K1, then V(j), K(j+2) for j = 0, 1, ... (K(j+2) only while it exists),
+// each as two consecutive positions (feature halves).  Tile position p of
+// that sequence -> (is_v, tile).
 __device__ __forceinline__ void ring_item(int p, int n, bool& is_v, int& tile) {
   if (p < 2 && p < n) {
     is_v = false;
@@ -117,7 +123,7 @@ __global__ void __launch_bounds__(192, 1)
   const int off = Nk - Nq;  // causal: key visible iff key <= row + off
   const int n_kv = (Nk + C::BN - 1) / C::BN;
   const int n = CAUSAL ? causal_key_tiles(q0 + C::BM - 1, off, n_kv, C::BN) : n_kv;  // key tiles visited
-  const int n_items = 2 * n;  // ring positions: every K and every V once
+  const int n_items = 4 * n;  // ring positions: both halves of every K and every V once
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -162,12 +168,13 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(&ring_empty[slot], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         bool is_v;
         int tile;
-        ring_item(p, n, is_v, tile);
+        ring_item(p >> 1, n, is_v, tile);
+        const int half = p & 1;  // features [128 half, 128 half + 128)
         mbar_arrive_expect_tx(&ring_full[slot], C::KV_TILE);
         const int2 ck = sv.kcoord(tile * C::BN);
-        for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sRing + slot * C::KV_TILE + s * C::KV_SLAB, is_v ? &tm_v : &tm_k, &ring_full[slot], s * 64,
-                      ck.x, ck.y);
+        for (int s = 0; s < 2; ++s)
+          tma_load_3d(sRing + slot * C::KV_TILE + s * C::KV_SLAB, is_v ? &tm_v : &tm_k, &ring_full[slot],
+                      128 * half + 64 * s, ck.x, ck.y);
         issued = p + 1;
       }
       if (*abort_flag) {  // let every copy in flight land before the CTA exits
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, C::BN, BF16, false, false);  // K-major A and B
-      constexpr uint32_t kIdPV = idesc_f16(128, D, BF16, false, true);      // B (V) MN-major
+      constexpr uint32_t kIdPV = idesc_f16(128, 128, BF16, false, true);    // B (V) MN-major, one feature half
       const uint32_t sq = smem_u32(sQ);
       const uint32_t sring = smem_u32(sRing);
       // descriptors of Q and of ring slot 0 (K: K-major; V: MN-major), advanced per K-step
@@ -188,23 +195,30 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t dk0 = sdesc_sw128(sring, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sring, C::KV_SLAB, 1024);
       int pos = 0;  // next ring position to consume
-      // S(j) = Q K(j)^T into S buffer b: 16 k-steps of 16 features.
-      auto issue_s = [&](int b, int slot) {
-        const uint64_t dk = sdesc_advance(dk0, slot * C::KV_TILE);
+      // S(j) = Q K(j)^T into S buffer b: 16 k-steps of 16 features, the first
+      // 8 from K's half in ring slot k0, the last 8 from slot k1.
+      auto issue_s = [&](int b, int k0, int k1) {
+        const uint64_t dka = sdesc_advance(dk0, k0 * C::KV_TILE);
+        const uint64_t dkb = sdesc_advance(dk0, k1 * C::KV_TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t oa = (kk >> 2) * C::Q_SLAB + (kk & 3) * 32;
-          const uint32_t ob = (kk >> 2) * C::KV_SLAB + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S + 64 * b, sdesc_advance(dq, oa), sdesc_advance(dk, ob), kIdS, kk > 0);
+          const uint32_t ob = ((kk >> 2) & 1) * C::KV_SLAB + (kk & 3) * 32;
+          mma_ss(tmem + C::COL_S + 128 * b, sdesc_advance(dq, oa), sdesc_advance(kk < 8 ? dka : dkb, ob), kIdS,
+                 kk > 0);
         }
       };
-      // O += P(j) V(j): P read from S buffer b (16-bit pairs, 8 columns per 16 keys).
-      auto issue_pv = [&](int b, int slot, bool first) {
-        const uint64_t dv = sdesc_advance(dv0, slot * C::KV_TILE);
+      // O += P(j) V(j): P read from S buffer b (16-bit pairs, 8 columns per 16
+      // keys); O's feature half h from V's half in ring slot v_h.
+      auto issue_pv = [&](int b, int v0, int v1, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + C::COL_O, tmem + C::COL_S + 64 * b + kk * 8, sdesc_advance(dv, kk * 2048), kIdPV,
-                 !first || kk > 0);
+        for (int h = 0; h < 2; ++h) {
+          const uint64_t dv = sdesc_advance(dv0, (h ? v1 : v0) * C::KV_TILE);
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ts(tmem + C::COL_O + 128 * h, tmem + C::COL_S + 128 * b + kk * 8, sdesc_advance(dv, kk * 2048),
+                   kIdPV, !first || kk > 0);
+        }
       };
       auto take = [&](bool& ok) {  // wait for the next ring position; returns its slot
         const int slot = pos % C::NS;
@@ -214,29 +228,35 @@ __global__ void __launch_bounds__(192, 1)
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusTimeout);
       for (int j = 0; ok && j < n && j < 2; ++j) {  // S(0), S(1)
-        const int slot = take(ok);
+        const int k0 = take(ok);
+        const int k1 = ok ? take(ok) : 0;
         if (!ok) break;
         tc_fence_after();
-        issue_s(j, slot);
+        issue_s(j, k0, k1);
         mma_commit(&s_full[j]);
-        mma_commit(&ring_empty[slot]);
+        mma_commit(&ring_empty[k0]);
+        mma_commit(&ring_empty[k1]);
       }
       for (int j = 0; ok && j < n; ++j) {
         const int b = j & 1;
         if (!(ok = mbar_wait(&p_full[b], (uint32_t)((j >> 1) & 1), abort_flag, status, kStatusTimeout))) break;
-        const int vslot = take(ok);
+        const int v0 = take(ok);
+        const int v1 = ok ? take(ok) : 0;
         if (!ok) break;
         tc_fence_after();
-        issue_pv(b, vslot, j == 0);
-        mma_commit(&ring_empty[vslot]);
+        issue_pv(b, v0, v1, j == 0);
+        mma_commit(&ring_empty[v0]);
+        mma_commit(&ring_empty[v1]);
         mma_commit(pv_done);
         if (j + 2 < n) {  // S(j+2) reuses buffer b: in-order after PV(j), which reads P(j) there
-          const int kslot = take(ok);
+          const int k0 = take(ok);
+          const int k1 = ok ? take(ok) : 0;
           if (!ok) break;
           tc_fence_after();
-          issue_s(b, kslot);
+          issue_s(b, k0, k1);
           mma_commit(&s_full[b]);
-          mma_commit(&ring_empty[kslot]);
+          mma_commit(&ring_empty[k0]);
+          mma_commit(&ring_empty[k1]);
         }
       }
       mma_commit(ok ? o_full : drain);  // with no key tile this arrives at once
@@ -256,24 +276,24 @@ __global__ void __launch_bounds__(192, 1)
     float l = 0.f;
     float l_mma = 0.f;
     bool ok = true;
-    uint32_t keep[2] = {0u, 0u};  // dropout bits of the next tile, 32 keys per word
-    auto draw = [&](int j) { tile_keep_bits<2>(keep, j * C::BN, row, bh, drop.offset, drop.k0, drop.k1, drop.t); };
+    uint32_t keep[4] = {0u, 0u, 0u, 0u};  // dropout bits of the next tile, 32 keys per word
+    auto draw = [&](int j) { tile_keep_bits<4>(keep, j * C::BN, row, bh, drop.offset, drop.k0, drop.k1, drop.t); };
     if (DROP && n > 0) draw(0);
     for (int j = 0; j < n; ++j) {
       const int b = j & 1;
-      const uint32_t tS = lane_base + C::COL_S + 64 * b;
+      const uint32_t tS = lane_base + C::COL_S + 128 * b;
       if (!(ok = warp_wait(&s_full[b], (uint32_t)((j >> 1) & 1), abort_flag, status))) break;
       tc_fence_after();
-      float s[2][32];
-      tmem_ld32(tS, s[0]);
-      tmem_ld32(tS + 32, s[1]);
-      tmem_ld_wait(s[0]);
-      tmem_ld_wait(s[1]);
+      float s[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + 32 * cc, s[cc]);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(s[cc]);
       const int kbase = j * C::BN;
       const bool need_mask = (kbase + C::BN > Nk) || (CAUSAL && kbase + C::BN - 1 > q0 + off);
       if (need_mask) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc)
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int key = kbase + 32 * cc + i;
@@ -282,7 +302,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       float mx = s[0][0];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
+      for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) mx = max3(mx, s[cc][i], s[cc][i + 1]);
       const float m_new = fmaxf(m_ref, mx * scale_log2);
@@ -302,7 +322,7 @@ __global__ void __launch_bounds__(192, 1)
       uint64_t sum2 = f2_pack(0.f, 0.f);
       uint64_t sumr2 = f2_pack(0.f, 0.f);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {  // 32 scores -> 16 packed pairs -> 16 TMEM columns
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {

@@ -75,8 +75,7 @@ cudaError_t launch_forward_persistent(int d, bool causal, bool bf16, const FwdAr
 cudaError_t launch_forward_dropout(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 // Packed variable-length instances (a.lay.cu_q != nullptr), with or without dropout.
 cudaError_t launch_forward_varlen(int d, bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
-// Head dimension 256 (dense or packed, with or without dropout; no block mask):
-// K / V tensor maps with 64-row boxes.
+// Head dimension 256 (dense or packed, with or without dropout; no block mask).
 cudaError_t launch_forward256(bool causal, bool bf16, const FwdArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
