@@ -435,10 +435,12 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
         else:
             fa.fa_forward_dropout(q, k, v, o, lse, DROP_P, DROP_SEED, DROP_OFFSET, w.causal)
 
-    split = kind == "dense" and d != 256  # the strategy fa_backward takes
+    split = kind in ("dense", "blocksparse") and d != 256  # the strategy fa_backward takes
 
     def dkdv():
-        if split:
+        if split and kind == "blocksparse":
+            fa.fa_backward_dk_dv_blocksparse(q, k, v, do, lse, delta, dk, dv, md, w.causal)
+        elif split:
             fa.fa_backward_dk_dv(q, k, v, do, lse, delta, dk, dv, w.causal)
         elif kind == "dense":
             fa.fa_backward_dkdv(q, k, v, do, lse, delta, acc, dk, dv, w.causal)
@@ -459,7 +461,9 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
         if e: e[2].record(stream)
         dkdv()
         if e: e[3].record(stream)
-        if split:
+        if split and kind == "blocksparse":
+            fa.fa_backward_dq_blocksparse(q, k, v, do, lse, delta, dq, md, w.causal)
+        elif split:
             fa.fa_backward_dq(q, k, v, do, lse, delta, dq, w.causal)
         else:
             fa.fa_backward_dq_convert(flat(acc), flat(dq), scale=1.0 / math.sqrt(d))
@@ -487,9 +491,9 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
 
 def dkdv_factor(kind, w) -> float:
     """The dK/dV kernel's FLOPs in units of the forward's F: 2 (S^T, dP^T, dV, dK) where
-    the backward takes the split strategy (dense, d <= 128), 2.5 where that kernel also
-    forms the dQ partials."""
-    return 2.0 if kind == "dense" and w.d != 256 else 2.5
+    the backward takes the split strategy (dense layouts at d <= 128, with or without a
+    block mask), 2.5 where that kernel also forms the dQ partials."""
+    return 2.0 if kind in ("dense", "blocksparse") and w.d != 256 else 2.5
 
 
 def variant_flops(kind, w, bm):
@@ -555,7 +559,7 @@ def run_variant(args, world, rank, local, kind):
     fa.fa_device_status()
     elem = q.numel() * 2
     peak = float(peaks["bf16_tflops"])
-    dkdv = 2.5 * F / (parts[2] * 1e-3) / 1e12
+    dkdv = dkdv_factor(kind, w) * F / (parts[2] * 1e-3) / 1e12
     fwd = F / (parts[0] * 1e-3) / 1e12
     if kind == "varlen":
         cpu, heads, spent, threads = oracle_varlen_sample(w, args.cpu_budget)
@@ -575,8 +579,8 @@ def run_variant(args, world, rank, local, kind):
         data = "synthetic (seeded N(0,1) Q, K, V, dO; seeded random block mask; no dataset)"
         cfg = {"density": w.density, "kept_blocks": int(bm.sum()), "mask_heads": int(bm.shape[0]),
                "flop_count": "F = 4*d per (query, key) pair inside kept blocks; fwd+bwd = 2.5 F"}
-        kern = "fa_bwd_dkdv_kernel<128,non-causal,bf16,sparse>"
-        alg = "10*d per (query, key) pair of the kept blocks (5 GEMMs), per launch"
+        kern = "fa_bwd_dkdv_split_kernel<128,non-causal,bf16,sparse>"
+        alg = "8*d per (query, key) pair of the kept blocks (4 GEMMs: S^T, dP^T, dV, dK), per launch"
         h2d_extra = md.numel()
         what = "under the block mask"
     else:
@@ -598,8 +602,10 @@ def run_variant(args, world, rank, local, kind):
                        **cfg),
         "fwd_tflops": round(fwd, 1), "fwd_frac_of_peak": round(fwd / peak, 4),
         "fwdbwd_frac_of_peak": round(value / peak, 4),
-        "kernel_ms": {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
-                      "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)},
+        "kernel_ms": ({"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
+                       "bwd_dk_dv": round(parts[2], 4), "bwd_dq": round(parts[3], 4)} if kind == "blocksparse" else
+                      {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
+                       "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)}),
         "roofline": {"bound": "tensor", "kernel": kern,
                      "achieved": round(dkdv, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(dkdv / peak, 4),
                      "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic": alg},

@@ -6,7 +6,8 @@ Importing this package does not load the library; the first call does, and
 fails loudly if it has not been built.
 """
 from .api import (FAError, backward, fa_backward, fa_backward_dkdv, fa_backward_dq_convert,  # noqa: F401
-                  fa_backward_dk_dv, fa_backward_dq,
+                  fa_backward_dk_dv, fa_backward_dq, fa_backward_dk_dv_blocksparse,
+                  fa_backward_dq_blocksparse,
                   fa_backward_noalloc, fa_decode_workspace_size, fa_forward_decode, forward_decode,
                   fa_forward_blocksparse, fa_backward_blocksparse, fa_backward_dkdv_blocksparse,
                   fa_forward_dropout, fa_backward_dropout, fa_backward_dkdv_dropout, fa_dropout_keep_mask,

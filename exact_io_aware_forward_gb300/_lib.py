@@ -34,6 +34,9 @@ SIGNATURES = {
     "fa_backward_dq_convert": (_I, [_P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_backward_dk_dv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_backward_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_backward_dk_dv_blocksparse": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                           _P]),
+    "fa_backward_dq_blocksparse": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
     "fa_forward_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),

@@ -344,6 +344,32 @@ def fa_backward_dq(q, k, v, do, lse, delta, dq, causal=False, scale=None, stream
                                                   _scale(scale, d), _stream(stream)))
 
 
+def fa_backward_dk_dv_blocksparse(q, k, v, do, lse, delta, dk, dv, block_mask, causal=False, scale=None,
+                                  stream=None) -> None:
+    """Split backward restricted to the kept blocks: dK and dV."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    mptr, mheads = _block_mask(block_mask, B, H, N)
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dk", dk, q.shape, dt), _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_dk_dv_blocksparse", lib().fa_backward_dk_dv_blocksparse(
+        *args, mptr, mheads, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), _stream(stream)))
+
+
+def fa_backward_dq_blocksparse(q, k, v, do, lse, delta, dq, block_mask, causal=False, scale=None,
+                               stream=None) -> None:
+    """Split backward restricted to the kept blocks: dQ."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    mptr, mheads = _block_mask(block_mask, B, H, N)
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dq", dq, q.shape, dt)]
+    _check("fa_backward_dq_blocksparse", lib().fa_backward_dq_blocksparse(
+        *args, mptr, mheads, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), _stream(stream)))
+
+
 def fa_backward_dq_convert(dq_accum, dq, scale=None, stream=None) -> None:
     B, H, N, d = _shape(dq)
     args = [_bhnd("dq_accum", dq_accum, dq.shape, torch.float32), _bhnd("dq", dq)]

@@ -249,8 +249,8 @@ fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, 
 // The two stages of the split backward: dK and dV (want_dq false) or dQ
 // (want_dq true), each recomputing P and dP; dense layouts, d in {64, 96, 128}.
 fa_status run_split(const Shape& s, bool want_dq, const void* q, const void* k, const void* v, const void* dO,
-                    const float* lse, const float* delta, void* dq, void* dk, void* dv, int causal, float scale,
-                    void* stream) {
+                    const float* lse, const float* delta, void* dq, void* dk, void* dv, const uint8_t* block_mask,
+                    int mask_heads, int causal, float scale, void* stream) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
   if (s.varlen() || s.width() == 256) return FA_ERR_UNSUPPORTED;
@@ -271,6 +271,8 @@ fa_status run_split(const Shape& s, bool want_dq, const void* q, const void* k, 
   a.dh = s.d;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
+  a.block_mask = block_mask;
+  a.mask_heads = mask_heads;
   a.status = status_word();
   if (!a.status) return FA_ERR_CUDA;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -320,15 +322,17 @@ fa_status run_backward(const Shape& s, const void* q, const void* k, const void*
   float* delta = static_cast<float*>(workspace);
   float* dq_accum =
       reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)s.q_rows() * sizeof(float)));
-  // Dense attention without a block mask or dropout at d <= 128 takes the
-  // split backward (dQ by its own kernel, no accumulator); the rest
+  // Dense layouts at d <= 128 without dropout, with or without a block mask,
+  // take the split backward (dQ by its own kernel, no accumulator); the rest
   // accumulates dQ in the dK / dV kernel.
-  const bool split = !s.varlen() && !block_mask && !(drop && drop->t > 0) && s.width() != 256;
+  const bool split = !s.varlen() && !(drop && drop->t > 0) && s.width() != 256;
   if (split) {
     if ((st = run_preprocess(s, o, dO, delta, nullptr, stream)) != FA_OK) return st;
-    if ((st = run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, causal, scale, stream)) != FA_OK)
+    if ((st = run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, block_mask, mask_heads, causal, scale,
+                        stream)) != FA_OK)
       return st;
-    return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, causal, scale, stream);
+    return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, block_mask, mask_heads, causal, scale,
+                     stream);
   }
   if ((st = run_preprocess(s, o, dO, delta, dq_accum, stream)) != FA_OK) return st;
   if ((st = run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, causal, scale, stream,
@@ -537,7 +541,7 @@ fa_status fa_backward_dk_dv(const void* q, const void* k, const void* v, const v
   Shape s;
   const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
   if (st != FA_OK) return st;
-  return run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, causal, scale, stream);
+  return run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, nullptr, 1, causal, scale, stream);
 }
 
 fa_status fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
@@ -546,7 +550,29 @@ fa_status fa_backward_dq(const void* q, const void* k, const void* v, const void
   Shape s;
   const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
   if (st != FA_OK) return st;
-  return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, causal, scale, stream);
+  return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, nullptr, 1, causal, scale, stream);
+}
+
+fa_status fa_backward_dk_dv_blocksparse(const void* q, const void* k, const void* v, const void* dO,
+                                        const float* lse, const float* delta, void* dk, void* dv,
+                                        const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d,
+                                        int dtype, int causal, float scale, void* stream) {
+  Shape s;
+  fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_block_mask(block_mask, mask_heads, B, H)) != FA_OK) return st;
+  return run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, block_mask, mask_heads, causal, scale, stream);
+}
+
+fa_status fa_backward_dq_blocksparse(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                     const float* delta, void* dq, const uint8_t* block_mask, int mask_heads, int B,
+                                     int H, int N, int d, int dtype, int causal, float scale, void* stream) {
+  Shape s;
+  fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  if ((st = check_block_mask(block_mask, mask_heads, B, H)) != FA_OK) return st;
+  return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, block_mask, mask_heads, causal, scale,
+                   stream);
 }
 
 fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,

@@ -95,13 +95,14 @@ struct DkdvSplitCfg : SplitCfg<D> {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE>
 __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     fa_bwd_dkdv_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                              const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                              const float* __restrict__ lse, const float* __restrict__ delta, int N, int BH, int dh,
-                             float scale, float scale_log2, int group, unsigned int* status) {
+                             float scale, float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads,
+                             int group, unsigned int* status) {
   using C = DkdvSplitCfg<D>;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
@@ -143,7 +144,24 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
   const int kv0 = j * C::BKV;
   const int n_q = (N + C::BQ - 1) / C::BQ;
   const int i_begin = CAUSAL ? kv0 / C::BQ : 0;  // first query tile with a query >= kv0
-  const int n_it = n_q - i_begin;
+  // Block-sparse: query tile i meets this key tile iff its mask byte
+  // (128 x 128 blocks, [mask_heads, n_q, n_q]) is non-zero.
+  const uint8_t* mcol = SPARSE ? block_mask + (long long)(mask_heads == 1 ? 0 : bh) * n_q * n_q + j : nullptr;
+  auto next_tile = [&](int i) {  // the first visited query tile >= i (n_q if none)
+    if constexpr (SPARSE) {
+      while (i < n_q && mcol[(long long)i * n_q] == 0) ++i;
+    }
+    return i;
+  };
+  int* n_visit = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+  if (SPARSE && warp == 0) {  // count the visited query tiles, 32 at a time
+    int cnt = 0;
+    for (int b = i_begin; b < n_q; b += 32) {
+      const int i = b + lane;
+      cnt += __popc(__ballot_sync(0xffffffffu, i < n_q && mcol[(long long)i * n_q] != 0));
+    }
+    if (lane == 0) *n_visit = cnt;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -180,6 +198,7 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int n_it = SPARSE ? *n_visit : n_q - i_begin;  // query tiles visited
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -190,12 +209,14 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
         tma_load_3d(sV + s * C::SLAB, &tm_v, kv_full, s * 64, kv0, bh);
       }
       int issued = 0;
+      int i_sp = next_tile(i_begin);  // block-sparse: the query tile of iteration it
       for (int it = 0; it < n_it; ++it) {
         const int b = it % C::QS;
         const uint32_t use = (uint32_t)(it / C::QS);
         if (!mbar_wait(&q_empty[b], (use & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         mbar_arrive_expect_tx(&q_full[b], 2 * C::TILE);
-        const int q0 = (i_begin + it) * C::BQ;
+        const int q0 = (SPARSE ? i_sp : i_begin + it) * C::BQ;
+        if constexpr (SPARSE) i_sp = next_tile(i_sp + 1);
         for (int s = 0; s < C::SLABS; ++s) {
           tma_load_3d(sQ + b * C::TILE + s * C::SLAB, &tm_q, &q_full[b], s * 64, q0, bh);
           tma_load_3d(sDO + b * C::TILE + s * C::SLAB, &tm_do, &q_full[b], s * 64, q0, bh);
@@ -327,10 +348,11 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
         pre_d = delta[row0 + q];
       }
     };
-    if (n_it > 0) fetch(i_begin);
+    int i_sp = next_tile(i_begin);  // block-sparse: the query tile of iteration it
+    if (n_it > 0) fetch(SPARSE ? i_sp : i_begin);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int i = i_begin + it;
+      const int i = SPARSE ? i_sp : i_begin + it;
       const int q0 = i * C::BQ;
       // the staged values of the previous tile have been read by every warp of the warpgroup
       if (it > 0 && !(ok = warp_wait(&ld_empty[h], (it - 1) & 1, abort_flag, status))) break;
@@ -341,7 +363,9 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ld_full[h]);
       if (!(ok = warp_wait(&ld_full[h], it & 1, abort_flag, status))) break;
-      if (it + 1 < n_it) fetch(i + 1);
+      int i_next = i + 1;
+      if constexpr (SPARSE) i_next = next_tile(i + 1);
+      if (it + 1 < n_it) fetch(i_next);
       // ---- pass 1: S^T into registers (S^T(i+1) may then be issued), P^T into shared memory
       if (!(ok = warp_wait(s_full, it & 1, abort_flag, status))) break;
       tc_fence_after();
@@ -423,6 +447,7 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
         mbar_arrive(ds_full);
         mbar_arrive(&ld_empty[h]);
       }
+      if constexpr (SPARSE) i_sp = i_next;
     }
     // ------------------------------------------------------------ epilogue
     // Warpgroups 0 and 1 stage the two 64-feature halves of dV in the Q
@@ -485,12 +510,13 @@ struct DqCfg : SplitCfg<D> {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      void* __restrict__ dq, const float* __restrict__ lse, const float* __restrict__ delta, int N,
-                     int BH, int n_qblocks, int dh, float scale, float scale_log2, int group, unsigned int* status) {
+                     int BH, int n_qblocks, int dh, float scale, float scale_log2,
+                     const uint8_t* __restrict__ block_mask, int mask_heads, int group, unsigned int* status) {
   using C = DqCfg<D>;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
@@ -528,7 +554,22 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   const int qb = n_qblocks - 1 - within / heads;
   const int q0 = qb * C::BQ;
   const int n_kv = (N + C::BKV - 1) / C::BKV;
-  const int n = CAUSAL ? causal_key_tiles(q0 + C::BQ - 1, 0, n_kv, C::BKV) : n_kv;  // key tiles visited
+  const int n_k = CAUSAL ? causal_key_tiles(q0 + C::BQ - 1, 0, n_kv, C::BKV) : n_kv;  // key tiles in range
+  // Block-sparse: key tile j is visited iff this query tile's mask byte for it is non-zero.
+  const uint8_t* mrow =
+      SPARSE ? block_mask + (long long)(mask_heads == 1 ? 0 : bh) * n_kv * n_kv + (long long)qb * n_kv : nullptr;
+  auto next_tile = [&](int j) {  // the first visited key tile >= j (n_k if none)
+    if constexpr (SPARSE) {
+      while (j < n_k && mrow[j] == 0) ++j;
+    }
+    return j;
+  };
+  int* n_visit = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
+  if (SPARSE && warp == 0) {  // count the visited key tiles, 32 at a time
+    int cnt = 0;
+    for (int b = 0; b < n_k; b += 32) cnt += __popc(__ballot_sync(0xffffffffu, b + lane < n_k && mrow[b + lane] != 0));
+    if (lane == 0) *n_visit = cnt;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -566,6 +607,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int n = SPARSE ? *n_visit : n_k;  // key tiles visited
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -576,19 +618,19 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         tma_load_3d(sDO + s * C::SLAB, &tm_do, q_full, s * 64, q0, bh);
       }
       int k_issued = 0, v_issued = 0;
-      for (int jt = 0; jt < n; ++jt) {  // K_0, V_0, K_1, V_1, ...
+      for (int jt = 0, j = next_tile(0); jt < n; ++jt, j = next_tile(j + 1)) {  // K, V of each visited tile
         const int ks = jt % C::NK, vs = jt % C::NV;
         if (!mbar_wait(&k_empty[ks], ((jt / C::NK) & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         mbar_arrive_expect_tx(&k_full[ks], C::TILE);
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sK + ks * C::TILE + s * C::SLAB, &tm_k, &k_full[ks], s * 64, jt * C::BKV, bh);
+          tma_load_3d(sK + ks * C::TILE + s * C::SLAB, &tm_k, &k_full[ks], s * 64, (SPARSE ? j : jt) * C::BKV, bh);
         k_issued = jt + 1;
         // V slot 1 holds the staged Q until warpgroup 0 has copied it into TMEM
         if (jt == 1 && !mbar_wait(qa_full, 0, abort_flag, status, kStatusTimeout)) break;
         if (!mbar_wait(&v_empty[vs], ((jt / C::NV) & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         mbar_arrive_expect_tx(&v_full[vs], C::TILE);
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sV + vs * C::TILE + s * C::SLAB, &tm_v, &v_full[vs], s * 64, jt * C::BKV, bh);
+          tma_load_3d(sV + vs * C::TILE + s * C::SLAB, &tm_v, &v_full[vs], s * 64, (SPARSE ? j : jt) * C::BKV, bh);
         v_issued = jt + 1;
       }
       if (*abort_flag) {
@@ -702,8 +744,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
     const uint64_t nl2 = f2_pack(nl, nl);
     const uint64_t nd2 = f2_pack(nd, nd);
-    for (int jt = 0; ok && jt < n; ++jt) {
-      const int kb = jt * C::BKV + KW * h;  // first key of this warpgroup's columns
+    for (int jt = 0, j = next_tile(0); ok && jt < n; ++jt, j = next_tile(j + 1)) {
+      const int kb = (SPARSE ? j : jt) * C::BKV + KW * h;  // first key of this warpgroup's columns
       if (!(ok = warp_wait(s_full, jt & 1, abort_flag, status))) break;
       tc_fence_after();
       float p[NC][16];
@@ -778,6 +820,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     // [FW h, FW (h + 1)) of its row, those below dh.
     constexpr int FW = D / C::CWG;
     if (ok) ok = warp_wait(dq_full, 0, abort_flag, status);
+    if constexpr (SPARSE) {  // dense tiles always visit at least one key tile
+      if (ok && n == 0 && FW * h < dh && q < N) {  // no visited key tile (an empty mask row): dQ = 0
+        uint4* drow = reinterpret_cast<uint4*>(dq) + frow * (dh / 8) + FW * h / 8;
+#pragma unroll
+        for (int u = 0; u < FW / 8; ++u) drow[u] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     if (ok && n > 0 && FW * h < dh) {
       tc_fence_after();
       uint4* drow = reinterpret_cast<uint4*>(dq) + frow * (dh / 8) + FW * h / 8;
@@ -806,10 +855,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE>
 cudaError_t launch_dkdv_split_t(const SplitArgs& a, cudaStream_t stream) {
   using C = DkdvSplitCfg<D>;
-  auto kern = fa_bwd_dkdv_split_kernel<D, CAUSAL, BF16>;
+  auto kern = fa_bwd_dkdv_split_kernel<D, CAUSAL, BF16, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_kt = (a.N + C::BKV - 1) / C::BKV;
@@ -819,15 +868,15 @@ cudaError_t launch_dkdv_split_t(const SplitArgs& a, cudaStream_t stream) {
   const long long per_head = 4LL * a.N * D;
   const int group = (int)std::max(1LL, std::min(16LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.tm_dk, a.tm_dv, a.lse,
-                                                         a.delta, a.N, a.BH, a.dh, a.scale, a.scale_log2, group,
-                                                         a.status);
+                                                         a.delta, a.N, a.BH, a.dh, a.scale, a.scale_log2,
+                                                         a.block_mask, a.mask_heads, group, a.status);
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE>
 cudaError_t launch_dq_t(const SplitArgs& a, cudaStream_t stream) {
   using C = DqCfg<D>;
-  auto kern = fa_bwd_dq_kernel<D, CAUSAL, BF16>;
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL, BF16, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblocks = (a.N + C::BQ - 1) / C::BQ;
@@ -837,16 +886,18 @@ cudaError_t launch_dq_t(const SplitArgs& a, cudaStream_t stream) {
   const long long per_head = 4LL * a.N * D;
   const int group = (int)std::max(1LL, std::min(64LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dq, a.lse, a.delta, a.N,
-                                                         a.BH, n_qblocks, a.dh, a.scale, a.scale_log2, group,
-                                                         a.status);
+                                                         a.BH, n_qblocks, a.dh, a.scale, a.scale_log2, a.block_mask,
+                                                         a.mask_heads, group, a.status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_backward_dkdv_split(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream) {
-#define FA_SPLIT_CASE(DD, CC, BB) \
-  if (d == DD && causal == CC && bf16 == BB) return launch_dkdv_split_t<DD, CC, BB>(a, stream);
+#define FA_SPLIT_CASE(DD, CC, BB)                                                               \
+  if (d == DD && causal == CC && bf16 == BB)                                                   \
+    return a.block_mask ? launch_dkdv_split_t<DD, CC, BB, true>(a, stream)                      \
+                        : launch_dkdv_split_t<DD, CC, BB, false>(a, stream);
   FA_SPLIT_CASE(64, false, false)
   FA_SPLIT_CASE(64, false, true)
   FA_SPLIT_CASE(64, true, false)
@@ -860,8 +911,9 @@ cudaError_t launch_backward_dkdv_split(int d, bool causal, bool bf16, const Spli
 }
 
 cudaError_t launch_backward_dq(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream) {
-#define FA_DQ_CASE(DD, CC, BB) \
-  if (d == DD && causal == CC && bf16 == BB) return launch_dq_t<DD, CC, BB>(a, stream);
+#define FA_DQ_CASE(DD, CC, BB)                                                                   \
+  if (d == DD && causal == CC && bf16 == BB)                                                   \
+    return a.block_mask ? launch_dq_t<DD, CC, BB, true>(a, stream) : launch_dq_t<DD, CC, BB, false>(a, stream);
   FA_DQ_CASE(64, false, false)
   FA_DQ_CASE(64, false, true)
   FA_DQ_CASE(64, true, false)

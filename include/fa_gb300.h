@@ -108,12 +108,14 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  *   dS = P * (G V^T - D),  D_i = sum_c dO_ic O_ic  ( = rowsum(P * (G V^T)) ),
  *   dQ = s dS K,  dK = s dS^T Q,  dV = P^T G.
  * Two strategies for dQ, both exact (chosen per call, see below):
- *   - split (dense attention, d in {64, 96, 128}): fa_backward_preprocess
- *     with dq_accum = NULL, fa_backward_dk_dv, fa_backward_dq -- dQ by a
+ *   - split (dense layouts, d in {64, 96, 128}, with or without a block
+ *     mask, no dropout): fa_backward_preprocess with dq_accum = NULL,
+ *     fa_backward_dk_dv, fa_backward_dq (with a block mask:
+ *     fa_backward_dk_dv_blocksparse, fa_backward_dq_blocksparse) -- dQ by a
  *     kernel of its own that recomputes P and dP, no float32 accumulator;
- *   - accumulated (d = 256): fa_backward_preprocess, fa_backward_dkdv,
- *     fa_backward_dq_convert -- dQ partials added into a float32
- *     accumulator by the dK / dV kernel.
+ *   - accumulated (d = 256, dropout, packed batches): fa_backward_preprocess,
+ *     fa_backward_dkdv, fa_backward_dq_convert -- dQ partials added into a
+ *     float32 accumulator by the dK / dV kernel.
  * All stages run in order on `stream`.  `workspace` must hold
  * fa_backward_workspace_size(B,H,N,d) bytes (else FA_ERR_WORKSPACE); its
  * contents on entry do not matter and are overwritten.
@@ -243,6 +245,22 @@ fa_status fa_backward_dk_dv(const void* q, const void* k, const void* v, const v
 fa_status fa_backward_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                          const float* delta, void* dq, int B, int H, int N, int d, int dtype, int causal, float scale,
                          void* stream);
+
+/*
+ * The split backward restricted to the kept blocks of block_mask (the
+ * whole-block skip of the tutorial's section 06 applied to both kernels;
+ * mask arguments and errors as fa_forward_blocksparse, the rest as
+ * fa_backward_dk_dv / fa_backward_dq).  fa_backward_dk_dv_blocksparse: a key
+ * block kept by no query block gets dK = dV = 0.  fa_backward_dq_blocksparse:
+ * a query block that keeps no key block gets dQ = 0.
+ */
+fa_status fa_backward_dk_dv_blocksparse(const void* q, const void* k, const void* v, const void* dO,
+                                        const float* lse, const float* delta, void* dk, void* dv,
+                                        const uint8_t* block_mask, int mask_heads, int B, int H, int N, int d,
+                                        int dtype, int causal, float scale, void* stream);
+fa_status fa_backward_dq_blocksparse(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                     const float* delta, void* dq, const uint8_t* block_mask, int mask_heads, int B,
+                                     int H, int N, int d, int dtype, int causal, float scale, void* stream);
 
 /*
  * Packed variable-length batches.  B sequences of different lengths laid end
