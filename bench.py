@@ -435,11 +435,13 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
         else:
             fa.fa_forward_dropout(q, k, v, o, lse, DROP_P, DROP_SEED, DROP_OFFSET, w.causal)
 
-    split = kind in ("dense", "blocksparse") and d != 256  # the strategy fa_backward takes
+    split = kind in ("dense", "blocksparse", "varlen") and d != 256  # the strategy fa_backward takes
 
     def dkdv():
         if split and kind == "blocksparse":
             fa.fa_backward_dk_dv_blocksparse(q, k, v, do, lse, delta, dk, dv, md, w.causal)
+        elif split and kind == "varlen":
+            fa.fa_backward_dk_dv_varlen(q, k, v, do, lse, delta, dk, dv, cu_q, cu_k, maxlen, maxlen, w.causal)
         elif split:
             fa.fa_backward_dk_dv(q, k, v, do, lse, delta, dk, dv, w.causal)
         elif kind == "dense":
@@ -463,6 +465,8 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
         if e: e[3].record(stream)
         if split and kind == "blocksparse":
             fa.fa_backward_dq_blocksparse(q, k, v, do, lse, delta, dq, md, w.causal)
+        elif split and kind == "varlen":
+            fa.fa_backward_dq_varlen(q, k, v, do, lse, delta, dq, cu_q, cu_k, maxlen, maxlen, w.causal)
         elif split:
             fa.fa_backward_dq(q, k, v, do, lse, delta, dq, w.causal)
         else:
@@ -491,9 +495,10 @@ def measure_variant(dev, kind, w, steps, warmup, sampler=None):
 
 def dkdv_factor(kind, w) -> float:
     """The dK/dV kernel's FLOPs in units of the forward's F: 2 (S^T, dP^T, dV, dK) where
-    the backward takes the split strategy (dense layouts at d <= 128, with or without a
-    block mask), 2.5 where that kernel also forms the dQ partials."""
-    return 2.0 if kind in ("dense", "blocksparse") and w.d != 256 else 2.5
+    the backward takes the split strategy (d <= 128 without dropout: dense layouts with or without a
+    block mask, and packed batches), 2.5 where that kernel also forms the dQ partials (d = 256,
+    dropout)."""
+    return 2.0 if kind in ("dense", "blocksparse", "varlen") and w.d != 256 else 2.5
 
 
 def variant_flops(kind, w, bm):
@@ -570,8 +575,8 @@ def run_variant(args, world, rank, local, kind):
         data = "synthetic (seeded N(0,1) packed Q, K, V, dO; seeded uniform sequence lengths; no dataset)"
         cfg = {"B": w.B, "lengths": list(w.lengths), "total_tokens": int(sum(w.lengths)),
                "flop_count": "F = 4*d*H per (query, key) pair of every sequence (causal: N(N+1)/2 pairs)"}
-        kern = "fa_bwd_dkdv_kernel<128,causal,bf16,varlen>"
-        alg = "10*d*H per (query, key) pair of every sequence (5 GEMMs), per launch"
+        kern = "fa_bwd_dkdv_split_kernel<128,causal,bf16,varlen>"
+        alg = "8*d*H per (query, key) pair of every sequence (4 GEMMs: S^T, dP^T, dV, dK), per launch"
         h2d_extra = 2 * 4 * (w.B + 1)
         what = "(the shortest sequences first)"
     elif kind == "blocksparse":
@@ -603,7 +608,7 @@ def run_variant(args, world, rank, local, kind):
         "fwd_tflops": round(fwd, 1), "fwd_frac_of_peak": round(fwd / peak, 4),
         "fwdbwd_frac_of_peak": round(value / peak, 4),
         "kernel_ms": ({"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
-                       "bwd_dk_dv": round(parts[2], 4), "bwd_dq": round(parts[3], 4)} if kind == "blocksparse" else
+                       "bwd_dk_dv": round(parts[2], 4), "bwd_dq": round(parts[3], 4)} if kind != "dropout" else
                       {"fa_fwd": round(parts[0], 4), "bwd_preprocess": round(parts[1], 4),
                        "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)}),
         "roofline": {"bound": "tensor", "kernel": kern,

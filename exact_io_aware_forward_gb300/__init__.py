@@ -12,6 +12,7 @@ from .api import (FAError, backward, fa_backward, fa_backward_dkdv, fa_backward_
                   fa_forward_blocksparse, fa_backward_blocksparse, fa_backward_dkdv_blocksparse,
                   fa_forward_dropout, fa_backward_dropout, fa_backward_dkdv_dropout, fa_dropout_keep_mask,
                   fa_forward_varlen, fa_backward_varlen, fa_backward_varlen_workspace_size, forward_varlen,
-                  backward_varlen, fa_backward_dkdv_varlen, fa_selftest_wait_timeout,
+                  backward_varlen, fa_backward_dkdv_varlen, fa_backward_dk_dv_varlen, fa_backward_dq_varlen,
+                  fa_selftest_wait_timeout,
                   fa_backward_preprocess, fa_backward_workspace_size, fa_device_status, fa_forward,
                   fa_score_blocks, forward)

@@ -53,6 +53,9 @@ SIGNATURES = {
                                 _F, _U64, _U32, _P, _S, _P]),
     "fa_backward_dkdv_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                      _I, _F, _F, _U64, _U32, _P]),
+    "fa_backward_dk_dv_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                      _F, _P]),
+    "fa_backward_dq_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_selftest_wait_timeout": (_I, [_P]),
     "fa_device_status": (_I, [_P]),
     "fa_score_blocks": (_I, [_P, ctypes.POINTER(_U64), ctypes.POINTER(_U64), _I]),

@@ -234,6 +234,33 @@ def fa_backward_dkdv_varlen(q, k, v, do, lse, delta, dq_accum, dk, dv, cu_seqlen
         _scale(scale, d), float(dropout_p), seed, offset, _stream(stream)))
 
 
+def fa_backward_dk_dv_varlen(q, k, v, do, lse, delta, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                             max_seqlen_k, causal=False, scale=None, stream=None) -> None:
+    """Split backward of a packed batch: dK and dV (no dQ work)."""
+    B, H, d, Tq, Tk = _varlen_args(q, k, cu_seqlens_q, cu_seqlens_k)
+    dt = q.dtype
+    args = [_bhnd("q", q), _bhnd("k", k, k.shape, dt), _bhnd("v", v, k.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (Tq, H), torch.float32), _bhnd("delta", delta, (Tq, H), torch.float32),
+            _bhnd("dk", dk, k.shape, dt), _bhnd("dv", dv, k.shape, dt), cu_seqlens_q.data_ptr(),
+            cu_seqlens_k.data_ptr()]
+    _check("fa_backward_dk_dv_varlen", lib().fa_backward_dk_dv_varlen(
+        *args, B, H, int(max_seqlen_q), int(max_seqlen_k), Tq, Tk, d, _DTYPE_CODE[dt], int(bool(causal)),
+        _scale(scale, d), _stream(stream)))
+
+
+def fa_backward_dq_varlen(q, k, v, do, lse, delta, dq, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                          causal=False, scale=None, stream=None) -> None:
+    """Split backward of a packed batch: dQ by its own kernel."""
+    B, H, d, Tq, Tk = _varlen_args(q, k, cu_seqlens_q, cu_seqlens_k)
+    dt = q.dtype
+    args = [_bhnd("q", q), _bhnd("k", k, k.shape, dt), _bhnd("v", v, k.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (Tq, H), torch.float32), _bhnd("delta", delta, (Tq, H), torch.float32),
+            _bhnd("dq", dq, q.shape, dt), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr()]
+    _check("fa_backward_dq_varlen", lib().fa_backward_dq_varlen(
+        *args, B, H, int(max_seqlen_q), int(max_seqlen_k), Tq, Tk, d, _DTYPE_CODE[dt], int(bool(causal)),
+        _scale(scale, d), _stream(stream)))
+
+
 def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False, scale=None,
                    dropout_p=0.0, seed=0, offset=0, stream=None):
     """Return (O [total_q, H, d], LSE [total_q, H]) for packed sequences."""

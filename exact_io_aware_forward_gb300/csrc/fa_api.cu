@@ -253,7 +253,7 @@ fa_status run_split(const Shape& s, bool want_dq, const void* q, const void* k, 
                     int mask_heads, int causal, float scale, void* stream) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  if (s.varlen() || s.width() == 256) return FA_ERR_UNSUPPORTED;
+  if (s.width() == 256) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) || !aligned16(delta))
     return FA_ERR_INVALID_ARG;
   if (want_dq ? !aligned16(dq) : (!aligned16(dk) || !aligned16(dv))) return FA_ERR_INVALID_ARG;
@@ -264,9 +264,11 @@ fa_status run_split(const Shape& s, bool want_dq, const void* q, const void* k, 
   if (!want_dq && (!make_map(&a.tm_dk, dk, s, true, 128) || !make_map(&a.tm_dv, dv, s, true, 128)))
     return FA_ERR_CUDA;
   a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
   a.lse = lse;
   a.delta = delta;
-  a.N = s.lay.Nq;
+  a.lay = s.lay;
   a.BH = s.B * s.H;
   a.dh = s.d;
   a.scale = scale;
@@ -322,10 +324,10 @@ fa_status run_backward(const Shape& s, const void* q, const void* k, const void*
   float* delta = static_cast<float*>(workspace);
   float* dq_accum =
       reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)s.q_rows() * sizeof(float)));
-  // Dense layouts at d <= 128 without dropout, with or without a block mask,
-  // take the split backward (dQ by its own kernel, no accumulator); the rest
+  // d <= 128 without dropout (dense with or without a block mask, or packed)
+  // takes the split backward (dQ by its own kernel, no accumulator); the rest
   // accumulates dQ in the dK / dV kernel.
-  const bool split = !s.varlen() && !(drop && drop->t > 0) && s.width() != 256;
+  const bool split = !(drop && drop->t > 0) && s.width() != 256;
   if (split) {
     if ((st = run_preprocess(s, o, dO, delta, nullptr, stream)) != FA_OK) return st;
     if ((st = run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, block_mask, mask_heads, causal, scale,
@@ -492,6 +494,28 @@ fa_status fa_backward_dkdv_varlen(const void* q, const void* k, const void* v, c
   fa::DropParams dp;
   if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
   return run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, nullptr, 1, causal, scale, stream, &dp);
+}
+
+fa_status fa_backward_dk_dv_varlen(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                  const float* delta, void* dk, void* dv, const int* cu_seqlens_q,
+                                  const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k,
+                                  int total_q, int total_k, int d, int dtype, int causal, float scale, void* stream) {
+  Shape s;
+  const fa_status st = varlen_shape(cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, max_seqlen_k, total_q, total_k,
+                                    d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, nullptr, 1, causal, scale, stream);
+}
+
+fa_status fa_backward_dq_varlen(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                const float* delta, void* dq, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                                int H, int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int d, int dtype,
+                                int causal, float scale, void* stream) {
+  Shape s;
+  const fa_status st = varlen_shape(cu_seqlens_q, cu_seqlens_k, B, H, max_seqlen_q, max_seqlen_k, total_q, total_k,
+                                    d, dtype, &s);
+  if (st != FA_OK) return st;
+  return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, nullptr, 1, causal, scale, stream);
 }
 
 fa_status fa_backward_preprocess(const void* o, const void* dO, float* delta, float* dq_accum, int B, int H,

@@ -95,14 +95,15 @@ struct DkdvSplitCfg : SplitCfg<D> {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN>
 __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     fa_bwd_dkdv_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                              const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                             const float* __restrict__ lse, const float* __restrict__ delta, int N, int BH, int dh,
-                             float scale, float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads,
-                             int group, unsigned int* status) {
+                             void* __restrict__ dk, void* __restrict__ dv, const float* __restrict__ lse,
+                             const float* __restrict__ delta, SeqLayout lay, int BH, int dh, float scale,
+                             float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads, int group,
+                             unsigned int* status) {
   using C = DkdvSplitCfg<D>;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
@@ -135,15 +136,21 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
   // Heads in groups of `group` (a group's Q and dO fit in about half of L2);
   // inside a group key tile 0 of every head (which meets every query tile
   // under the causal mask) first, then key tile 1, ...
-  const int n_kt = (N + C::BKV - 1) / C::BKV;
+  const int n_kt = (lay.Nk + C::BKV - 1) / C::BKV;  // key tiles of the longest sequence
   const int gi = blockIdx.x / (group * n_kt);
   const int heads = min(group, BH - gi * group);
   const int within = blockIdx.x - gi * group * n_kt;
   const int bh = gi * group + within % heads;
   const int j = within / heads;
   const int kv0 = j * C::BKV;
-  const int n_q = (N + C::BQ - 1) / C::BQ;
-  const int i_begin = CAUSAL ? kv0 / C::BQ : 0;  // first query tile with a query >= kv0
+  const SeqView sv = seq_view<VARLEN>(lay, bh);
+  if (VARLEN && !sv.ok && kv0 == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSeqlens);
+  if (kv0 >= sv.nk) return;  // past the end of a shorter (or rejected) sequence: the whole CTA leaves
+  const int Nq = sv.nq, Nk = sv.nk;
+  const int off = VARLEN ? Nk - Nq : 0;  // causal (bottom-right): key visible iff key <= query + off
+  const int n_q = (Nq + C::BQ - 1) / C::BQ;
+  // causal: the first query that sees key kv0 is kv0 - off
+  const int i_begin = CAUSAL ? (kv0 - off <= 0 ? 0 : (kv0 - off) / C::BQ) : 0;
   // Block-sparse: query tile i meets this key tile iff its mask byte
   // (128 x 128 blocks, [mask_heads, n_q, n_q]) is non-zero.
   const uint8_t* mcol = SPARSE ? block_mask + (long long)(mask_heads == 1 ? 0 : bh) * n_q * n_q + j : nullptr;
@@ -205,8 +212,9 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
       for (int s = 0; s < C::SLABS; ++s) {
-        tma_load_3d(sK + s * C::SLAB, &tm_k, kv_full, s * 64, kv0, bh);
-        tma_load_3d(sV + s * C::SLAB, &tm_v, kv_full, s * 64, kv0, bh);
+        const int2 ck = sv.kcoord(kv0);
+        tma_load_3d(sK + s * C::SLAB, &tm_k, kv_full, s * 64, ck.x, ck.y);
+        tma_load_3d(sV + s * C::SLAB, &tm_v, kv_full, s * 64, ck.x, ck.y);
       }
       int issued = 0;
       int i_sp = next_tile(i_begin);  // block-sparse: the query tile of iteration it
@@ -218,8 +226,9 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
         const int q0 = (SPARSE ? i_sp : i_begin + it) * C::BQ;
         if constexpr (SPARSE) i_sp = next_tile(i_sp + 1);
         for (int s = 0; s < C::SLABS; ++s) {
-          tma_load_3d(sQ + b * C::TILE + s * C::SLAB, &tm_q, &q_full[b], s * 64, q0, bh);
-          tma_load_3d(sDO + b * C::TILE + s * C::SLAB, &tm_do, &q_full[b], s * 64, q0, bh);
+          const int2 cq = sv.qcoord(q0);
+          tma_load_3d(sQ + b * C::TILE + s * C::SLAB, &tm_q, &q_full[b], s * 64, cq.x, cq.y);
+          tma_load_3d(sDO + b * C::TILE + s * C::SLAB, &tm_do, &q_full[b], s * 64, cq.x, cq.y);
         }
         issued = it + 1;
       }
@@ -330,7 +339,6 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     const int key = kv0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
-    const long long row0 = (long long)bh * N;
     float* sNL = sLD + h * 2 * QW;  // this warpgroup's columns: -LSE log2e, then -D
     float* sND = sNL + QW;
     // P^T of this warpgroup's queries: slab (QW h) / 64, from column (QW h) % 64
@@ -343,9 +351,9 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
       const int q = i * C::BQ + QW * h + r;
       pre_l = -pos_inf();
       pre_d = 0.f;
-      if (r < QW && q < N) {
-        pre_l = lse[row0 + q];
-        pre_d = delta[row0 + q];
+      if (r < QW && q < Nq) {
+        pre_l = lse[sv.qflat(q)];
+        pre_d = delta[sv.qflat(q)];
       }
     };
     int i_sp = next_tile(i_begin);  // block-sparse: the query tile of iteration it
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
       for (int sc = 0; sc < NC; ++sc) {
         const int col = 16 * sc;  // first query column of this chunk within the warpgroup's columns
         const int c0 = q0 + QW * h + col;
-        const bool need_mask = (CAUSAL && c0 < kv0 + C::BKV - 1) || (kv0 + C::BKV > N);
+        const bool need_mask = (CAUSAL && c0 + off < kv0 + C::BKV - 1) || (kv0 + C::BKV > Nk);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int c = 2 * e;
@@ -399,8 +407,8 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
             p1 = ex2_approx(x1);
           }
           if (need_mask) {
-            if (key >= N || (CAUSAL && key > c0 + c)) p0 = 0.f;
-            if (key >= N || (CAUSAL && key > c0 + c + 1)) p1 = 0.f;
+            if (key >= Nk || (CAUSAL && key > c0 + c + off)) p0 = 0.f;
+            if (key >= Nk || (CAUSAL && key > c0 + c + 1 + off)) p1 = 0.f;
           }
           p[sc][c] = p0;
           p[sc][c + 1] = p1;
@@ -459,16 +467,31 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     const bool has_half = 64 * half < D;
     if (ok && n_it > 0) ok = warp_wait(dkdv_done, 0, abort_flag, status);
     if (ok) tc_fence_after();
-    uint8_t* stage = (is_dk ? sDO : sQ) + half * C::SLAB;
-    if (ok && has_half)
-      stage_rows_from_tmem<64, BF16>(lane_base + (is_dk ? C::COL_DK : C::COL_DV) + 64 * half, stage, r,
-                                     is_dk ? scale : 1.f, n_it == 0);
-    fence_async_smem();
-    named_barrier_sync(1 + h, 128);
-    if (r == 0 && ok && has_half && !*abort_flag && 64 * half < dh) {
-      tma_store_3d(is_dk ? &tm_dk : &tm_dv, stage, 64 * half, kv0, bh);
-      tma_store_commit();
-      tma_store_wait_read();
+    if constexpr (VARLEN) {
+      // Packed batches: per-row stores (a tile's last rows can belong to the
+      // next sequence); a key tile no query sees writes zeros.
+      if (ok && has_half && 64 * half < dh) {
+        uint4* dst = reinterpret_cast<uint4*>(is_dk ? dk : dv) + sv.kflat(key) * (dh / 8) + 8 * half;
+        const int cols = min(64, dh - 64 * half);
+        if (n_it > 0) {
+          store_rows_from_tmem<64, BF16>(lane_base + (is_dk ? C::COL_DK : C::COL_DV) + 64 * half, dst, key < Nk,
+                                         is_dk ? scale : 1.f, cols);
+        } else if (key < Nk) {
+          for (int q = 0; q < cols / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    } else {
+      uint8_t* stage = (is_dk ? sDO : sQ) + half * C::SLAB;
+      if (ok && has_half)
+        stage_rows_from_tmem<64, BF16>(lane_base + (is_dk ? C::COL_DK : C::COL_DV) + 64 * half, stage, r,
+                                       is_dk ? scale : 1.f, n_it == 0);
+      fence_async_smem();
+      named_barrier_sync(1 + h, 128);
+      if (r == 0 && ok && has_half && !*abort_flag && 64 * half < dh) {
+        tma_store_3d(is_dk ? &tm_dk : &tm_dv, stage, 64 * half, kv0, bh);
+        tma_store_commit();
+        tma_store_wait_read();
+      }
     }
   }
 
@@ -510,12 +533,12 @@ struct DqCfg : SplitCfg<D> {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     void* __restrict__ dq, const float* __restrict__ lse, const float* __restrict__ delta, int N,
-                     int BH, int n_qblocks, int dh, float scale, float scale_log2,
+                     void* __restrict__ dq, const float* __restrict__ lse, const float* __restrict__ delta,
+                     SeqLayout lay, int BH, int n_qblocks, int dh, float scale, float scale_log2,
                      const uint8_t* __restrict__ block_mask, int mask_heads, int group, unsigned int* status) {
   using C = DqCfg<D>;
   constexpr float kLog2e = 1.4426950408889634f;
@@ -553,8 +576,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   const int bh = gi * group + within % heads;
   const int qb = n_qblocks - 1 - within / heads;
   const int q0 = qb * C::BQ;
-  const int n_kv = (N + C::BKV - 1) / C::BKV;
-  const int n_k = CAUSAL ? causal_key_tiles(q0 + C::BQ - 1, 0, n_kv, C::BKV) : n_kv;  // key tiles in range
+  const SeqView sv = seq_view<VARLEN>(lay, bh);
+  if (VARLEN && !sv.ok && q0 == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSeqlens);
+  if (q0 >= sv.nq) return;  // past the end of a shorter (or rejected) sequence: the whole CTA leaves
+  const int Nq = sv.nq, Nk = sv.nk;
+  const int off = VARLEN ? Nk - Nq : 0;  // causal (bottom-right): key visible iff key <= query + off
+  const int n_kv = (Nk + C::BKV - 1) / C::BKV;
+  const int n_k = CAUSAL ? causal_key_tiles(q0 + C::BQ - 1, off, n_kv, C::BKV) : n_kv;  // key tiles in range
   // Block-sparse: key tile j is visited iff this query tile's mask byte for it is non-zero.
   const uint8_t* mrow =
       SPARSE ? block_mask + (long long)(mask_heads == 1 ? 0 : bh) * n_kv * n_kv + (long long)qb * n_kv : nullptr;
@@ -614,23 +642,25 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, 2 * C::TILE);
       for (int s = 0; s < C::SLABS; ++s) {
-        tma_load_3d(sQ + s * C::SLAB, &tm_q, q_full, s * 64, q0, bh);
-        tma_load_3d(sDO + s * C::SLAB, &tm_do, q_full, s * 64, q0, bh);
+        const int2 cq = sv.qcoord(q0);
+        tma_load_3d(sQ + s * C::SLAB, &tm_q, q_full, s * 64, cq.x, cq.y);
+        tma_load_3d(sDO + s * C::SLAB, &tm_do, q_full, s * 64, cq.x, cq.y);
       }
       int k_issued = 0, v_issued = 0;
       for (int jt = 0, j = next_tile(0); jt < n; ++jt, j = next_tile(j + 1)) {  // K, V of each visited tile
         const int ks = jt % C::NK, vs = jt % C::NV;
         if (!mbar_wait(&k_empty[ks], ((jt / C::NK) & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         mbar_arrive_expect_tx(&k_full[ks], C::TILE);
+        const int2 ck = sv.kcoord((SPARSE ? j : jt) * C::BKV);
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sK + ks * C::TILE + s * C::SLAB, &tm_k, &k_full[ks], s * 64, (SPARSE ? j : jt) * C::BKV, bh);
+          tma_load_3d(sK + ks * C::TILE + s * C::SLAB, &tm_k, &k_full[ks], s * 64, ck.x, ck.y);
         k_issued = jt + 1;
         // V slot 1 holds the staged Q until warpgroup 0 has copied it into TMEM
         if (jt == 1 && !mbar_wait(qa_full, 0, abort_flag, status, kStatusTimeout)) break;
         if (!mbar_wait(&v_empty[vs], ((jt / C::NV) & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         mbar_arrive_expect_tx(&v_full[vs], C::TILE);
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sV + vs * C::TILE + s * C::SLAB, &tm_v, &v_full[vs], s * 64, (SPARSE ? j : jt) * C::BKV, bh);
+          tma_load_3d(sV + vs * C::TILE + s * C::SLAB, &tm_v, &v_full[vs], s * 64, ck.x, ck.y);
         v_issued = jt + 1;
       }
       if (*abort_flag) {
@@ -734,9 +764,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         if (lane == 0) mbar_arrive(qa_full);
       }
     }
-    const long long frow = (long long)bh * N + q;
+    const long long frow = sv.qflat(q);
     float nl = -pos_inf(), nd = 0.f;  // padding rows: P = 0
-    if (q < N) {
+    if (q < Nq) {
       const float lq = lse[frow];
       nl = lq == -pos_inf() ? -pos_inf() : -lq * kLog2e;
       nd = -delta[frow];
@@ -759,7 +789,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 #pragma unroll
       for (int sc = 0; sc < NC; ++sc) {
         const int k0 = kb + 16 * sc;
-        const bool need_mask = (CAUSAL && k0 + 15 > q0) || (k0 + 16 > N);
+        const bool need_mask = (CAUSAL && k0 + 15 > q0 + off) || (k0 + 16 > Nk);
 #pragma unroll
         for (int c = 0; c < 16; c += 2) {
           float x0, x1;
@@ -767,14 +797,14 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           float p0, p1;
           if ((c >> 1) < C::POLY_PAIRS) {
             exp2_poly2(x0, x1, p0, p1);
-            if (q >= N) p0 = p1 = 0.f;  // padding rows (the polynomial gives 2^-125, not 0, at -inf)
+            if (q >= Nq) p0 = p1 = 0.f;  // padding rows (the polynomial gives 2^-125, not 0, at -inf)
           } else {
             p0 = ex2_approx(x0);
             p1 = ex2_approx(x1);
           }
           if (need_mask) {
-            if (k0 + c >= N || (CAUSAL && k0 + c > q)) p0 = 0.f;
-            if (k0 + c + 1 >= N || (CAUSAL && k0 + c + 1 > q)) p1 = 0.f;
+            if (k0 + c >= Nk || (CAUSAL && k0 + c > q + off)) p0 = 0.f;
+            if (k0 + c + 1 >= Nk || (CAUSAL && k0 + c + 1 > q + off)) p1 = 0.f;
           }
           p[sc][c] = p0;
           p[sc][c + 1] = p1;
@@ -820,8 +850,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     // [FW h, FW (h + 1)) of its row, those below dh.
     constexpr int FW = D / C::CWG;
     if (ok) ok = warp_wait(dq_full, 0, abort_flag, status);
-    if constexpr (SPARSE) {  // dense tiles always visit at least one key tile
-      if (ok && n == 0 && FW * h < dh && q < N) {  // no visited key tile (an empty mask row): dQ = 0
+    if constexpr (SPARSE || VARLEN) {  // a square dense tile always visits at least one key tile
+      // no visited key tile (an empty mask row, or rows before the first key
+      // under a bottom-right causal mask): dQ = 0
+      if (ok && n == 0 && FW * h < dh && q < Nq) {
         uint4* drow = reinterpret_cast<uint4*>(dq) + frow * (dh / 8) + FW * h / 8;
 #pragma unroll
         for (int u = 0; u < FW / 8; ++u) drow[u] = make_uint4(0u, 0u, 0u, 0u);
@@ -840,7 +872,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       uint32_t pk[FW / 2];
 #pragma unroll
       for (int e = 0; e < FW / 2; ++e) pk[e] = pack2(v[2 * e] * scale, v[2 * e + 1] * scale, BF16);
-      if (q < N) {
+      if (q < Nq) {
 #pragma unroll
         for (int u = 0; u < FW / 8; ++u) drow[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
@@ -855,37 +887,37 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN>
 cudaError_t launch_dkdv_split_t(const SplitArgs& a, cudaStream_t stream) {
   using C = DkdvSplitCfg<D>;
-  auto kern = fa_bwd_dkdv_split_kernel<D, CAUSAL, BF16, SPARSE>;
+  auto kern = fa_bwd_dkdv_split_kernel<D, CAUSAL, BF16, SPARSE, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int n_kt = (a.N + C::BKV - 1) / C::BKV;
+  const int n_kt = (a.lay.Nk + C::BKV - 1) / C::BKV;  // packed batches: of the longest sequence
   const long long grid = (long long)n_kt * a.BH;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   // Q and dO of a head take 4 * N * D bytes; a group keeps them within ~64 MB of L2.
-  const long long per_head = 4LL * a.N * D;
+  const long long per_head = 4LL * a.lay.Nq * D;
   const int group = (int)std::max(1LL, std::min(16LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.tm_dk, a.tm_dv, a.lse,
-                                                         a.delta, a.N, a.BH, a.dh, a.scale, a.scale_log2,
-                                                         a.block_mask, a.mask_heads, group, a.status);
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.tm_dk, a.tm_dv, a.dk,
+                                                         a.dv, a.lse, a.delta, a.lay, a.BH, a.dh, a.scale,
+                                                         a.scale_log2, a.block_mask, a.mask_heads, group, a.status);
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN>
 cudaError_t launch_dq_t(const SplitArgs& a, cudaStream_t stream) {
   using C = DqCfg<D>;
-  auto kern = fa_bwd_dq_kernel<D, CAUSAL, BF16, SPARSE>;
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL, BF16, SPARSE, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int n_qblocks = (a.N + C::BQ - 1) / C::BQ;
+  const int n_qblocks = (a.lay.Nq + C::BQ - 1) / C::BQ;  // packed batches: of the longest sequence
   const long long grid = (long long)n_qblocks * a.BH;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   // K and V of a head take 4 * N * D bytes; a group keeps them within ~64 MB of L2.
-  const long long per_head = 4LL * a.N * D;
+  const long long per_head = 4LL * a.lay.Nk * D;
   const int group = (int)std::max(1LL, std::min(64LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dq, a.lse, a.delta, a.N,
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dq, a.lse, a.delta, a.lay,
                                                          a.BH, n_qblocks, a.dh, a.scale, a.scale_log2, a.block_mask,
                                                          a.mask_heads, group, a.status);
   return cudaGetLastError();
@@ -896,8 +928,9 @@ cudaError_t launch_dq_t(const SplitArgs& a, cudaStream_t stream) {
 cudaError_t launch_backward_dkdv_split(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream) {
 #define FA_SPLIT_CASE(DD, CC, BB)                                                               \
   if (d == DD && causal == CC && bf16 == BB)                                                   \
-    return a.block_mask ? launch_dkdv_split_t<DD, CC, BB, true>(a, stream)                      \
-                        : launch_dkdv_split_t<DD, CC, BB, false>(a, stream);
+    return a.lay.cu_q   ? launch_dkdv_split_t<DD, CC, BB, false, true>(a, stream)               \
+           : a.block_mask ? launch_dkdv_split_t<DD, CC, BB, true, false>(a, stream)             \
+                          : launch_dkdv_split_t<DD, CC, BB, false, false>(a, stream);
   FA_SPLIT_CASE(64, false, false)
   FA_SPLIT_CASE(64, false, true)
   FA_SPLIT_CASE(64, true, false)
@@ -913,7 +946,9 @@ cudaError_t launch_backward_dkdv_split(int d, bool causal, bool bf16, const Spli
 cudaError_t launch_backward_dq(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream) {
 #define FA_DQ_CASE(DD, CC, BB)                                                                   \
   if (d == DD && causal == CC && bf16 == BB)                                                   \
-    return a.block_mask ? launch_dq_t<DD, CC, BB, true>(a, stream) : launch_dq_t<DD, CC, BB, false>(a, stream);
+    return a.lay.cu_q   ? launch_dq_t<DD, CC, BB, false, true>(a, stream)                       \
+           : a.block_mask ? launch_dq_t<DD, CC, BB, true, false>(a, stream)                     \
+                          : launch_dq_t<DD, CC, BB, false, false>(a, stream);
   FA_DQ_CASE(64, false, false)
   FA_DQ_CASE(64, false, true)
   FA_DQ_CASE(64, true, false)

@@ -109,17 +109,20 @@ cudaError_t launch_backward_dkdv_varlen(int d, bool causal, bool bf16, const Bwd
 // keep[bh][i][j] = 1 if entry (bh, i, j) is kept, else 0 ([BH, Nq, Nk] bytes).
 cudaError_t launch_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, const DropParams& drop,
                                      cudaStream_t stream);
-// The backward pass with dQ computed by a kernel of its own (dense layouts,
-// with or without a block mask, no dropout): a dK / dV kernel and a dQ kernel
-// that both recompute P and dP on chip.
+// The backward pass with dQ computed by a kernel of its own (dense layouts
+// with or without a block mask, packed variable-length batches; no dropout):
+// a dK / dV kernel and a dQ kernel that both recompute P and dP on chip.
 struct SplitArgs {
   CUtensorMap tm_q, tm_do;         // box 64 columns x 128 rows
   CUtensorMap tm_k, tm_v;          // box 64 columns x 128 rows
   CUtensorMap tm_dk, tm_dv;        // box 64 columns x 128 rows (epilogue stores)
-  void* dq;                        // [B, H, N, dh] 16-bit
+  void* dq;                        // layout `lay` (query side), 16-bit
+  void* dk;                        // layout `lay` (key side): packed layouts store rows one by one
+  void* dv;
   const float* lse;
   const float* delta;
-  int N, BH, dh;
+  SeqLayout lay;
+  int BH, dh;
   float scale, scale_log2;
   const uint8_t* block_mask = nullptr;  // as FwdArgs (128 x 128 blocks); null = dense
   int mask_heads = 1;

@@ -108,12 +108,13 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  *   dS = P * (G V^T - D),  D_i = sum_c dO_ic O_ic  ( = rowsum(P * (G V^T)) ),
  *   dQ = s dS K,  dK = s dS^T Q,  dV = P^T G.
  * Two strategies for dQ, both exact (chosen per call, see below):
- *   - split (dense layouts, d in {64, 96, 128}, with or without a block
- *     mask, no dropout): fa_backward_preprocess with dq_accum = NULL,
- *     fa_backward_dk_dv, fa_backward_dq (with a block mask:
- *     fa_backward_dk_dv_blocksparse, fa_backward_dq_blocksparse) -- dQ by a
- *     kernel of its own that recomputes P and dP, no float32 accumulator;
- *   - accumulated (d = 256, dropout, packed batches): fa_backward_preprocess,
+ *   - split (d in {64, 96, 128} without dropout: dense layouts with or
+ *     without a block mask, packed batches): fa_backward_preprocess with
+ *     dq_accum = NULL, fa_backward_dk_dv, fa_backward_dq (with a block mask:
+ *     fa_backward_dk_dv_blocksparse, fa_backward_dq_blocksparse; packed:
+ *     fa_backward_dk_dv_varlen, fa_backward_dq_varlen) -- dQ by a kernel of
+ *     its own that recomputes P and dP, no float32 accumulator;
+ *   - accumulated (d = 256, dropout): fa_backward_preprocess,
  *     fa_backward_dkdv, fa_backward_dq_convert -- dQ partials added into a
  *     float32 accumulator by the dK / dV kernel.
  * All stages run in order on `stream`.  `workspace` must hold
@@ -305,6 +306,23 @@ fa_status fa_backward_dkdv_varlen(const void* q, const void* k, const void* v, c
                                   const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k,
                                   int total_q, int total_k, int d, int dtype, int causal, float scale, float p_drop,
                                   uint64_t seed, uint32_t offset, void* stream);
+/*
+ * The split backward of a packed batch (what fa_backward_varlen runs at
+ * d in {64, 96, 128} without dropout), after fa_backward_preprocess(o, dO,
+ * delta, NULL, 1, 1, total_q * H, d, ...): fa_backward_dk_dv_varlen writes
+ * dk, dv; fa_backward_dq_varlen writes dq (each needs no workspace).  As
+ * fa_backward_dk_dv / fa_backward_dq per sequence, with the layouts,
+ * offsets and bottom-right causal mask of fa_backward_varlen; d = 256 gives
+ * FA_ERR_UNSUPPORTED.
+ */
+fa_status fa_backward_dk_dv_varlen(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                   const float* delta, void* dk, void* dv, const int* cu_seqlens_q,
+                                   const int* cu_seqlens_k, int B, int H, int max_seqlen_q, int max_seqlen_k,
+                                   int total_q, int total_k, int d, int dtype, int causal, float scale, void* stream);
+fa_status fa_backward_dq_varlen(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                const float* delta, void* dq, const int* cu_seqlens_q, const int* cu_seqlens_k, int B,
+                                int H, int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int d, int dtype,
+                                int causal, float scale, void* stream);
 
 /*
  * Split-KV forward for few queries against many keys (decoding).

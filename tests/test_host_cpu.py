@@ -129,6 +129,7 @@ def test_dkdv_flop_factor_follows_the_backward_strategy():
     assert bench.dkdv_factor("dense", synth.W256) == 2.5
     assert bench.dkdv_factor("dropout", synth.C4) == 2.5
     assert bench.dkdv_factor("blocksparse", synth.S1) == 2.0
+    assert bench.dkdv_factor("varlen", synth.V1) == 2.0
 
 
 def _exp2_poly_f32(x):
