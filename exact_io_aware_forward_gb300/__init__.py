@@ -11,6 +11,7 @@ from .api import (FAError, backward, fa_backward, fa_backward_dkdv, fa_backward_
                   fa_backward_noalloc, fa_decode_workspace_size, fa_forward_decode, forward_decode,
                   fa_forward_blocksparse, fa_backward_blocksparse, fa_backward_dkdv_blocksparse,
                   fa_forward_dropout, fa_backward_dropout, fa_backward_dkdv_dropout, fa_dropout_keep_mask,
+                  fa_backward_dk_dv_dropout, fa_backward_dq_dropout,
                   fa_forward_varlen, fa_backward_varlen, fa_backward_varlen_workspace_size, forward_varlen,
                   backward_varlen, fa_backward_dkdv_varlen, fa_backward_dk_dv_varlen, fa_backward_dq_varlen,
                   fa_selftest_wait_timeout,

@@ -45,6 +45,9 @@ SIGNATURES = {
                                  _S, _P]),
     "fa_backward_dkdv_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32,
                                       _P]),
+    "fa_backward_dk_dv_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32,
+                                       _P]),
+    "fa_backward_dq_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32, _P]),
     "fa_dropout_keep_mask": (_I, [_P, _I, _I, _I, _F, _U64, _U32, _P]),
     "fa_forward_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32,
                                _P]),

@@ -160,6 +160,34 @@ def fa_backward_dkdv_dropout(q, k, v, do, lse, delta, dq_accum, dk, dv, p_drop, 
         _stream(stream)))
 
 
+def fa_backward_dk_dv_dropout(q, k, v, do, lse, delta, dk, dv, p_drop, seed, offset, causal=False, scale=None,
+                              stream=None) -> None:
+    """Split backward with dropout: dK and dV."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    seed, offset = _seed_offset(seed, offset)
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dk", dk, q.shape, dt), _bhnd("dv", dv, q.shape, dt)]
+    _check("fa_backward_dk_dv_dropout", lib().fa_backward_dk_dv_dropout(
+        *args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), float(p_drop), seed, offset,
+        _stream(stream)))
+
+
+def fa_backward_dq_dropout(q, k, v, do, lse, delta, dq, p_drop, seed, offset, causal=False, scale=None,
+                           stream=None) -> None:
+    """Split backward with dropout: dQ."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    seed, offset = _seed_offset(seed, offset)
+    args = [_bhnd("q", q), _bhnd("k", k, q.shape, dt), _bhnd("v", v, q.shape, dt), _bhnd("do", do, q.shape, dt),
+            _bhnd("lse", lse, (B, H, N), torch.float32), _bhnd("delta", delta, (B, H, N), torch.float32),
+            _bhnd("dq", dq, q.shape, dt)]
+    _check("fa_backward_dq_dropout", lib().fa_backward_dq_dropout(
+        *args, B, H, N, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), float(p_drop), seed, offset,
+        _stream(stream)))
+
+
 def fa_dropout_keep_mask(keep, p_drop, seed, offset, stream=None) -> None:
     """Write the keep mask ([BH, Nq, Nk] uint8 CUDA tensor, 1 = kept) the dropout entry points use."""
     if not isinstance(keep, torch.Tensor) or not keep.is_cuda or keep.dtype != torch.uint8 \

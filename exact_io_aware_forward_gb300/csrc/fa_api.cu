@@ -247,13 +247,16 @@ fa_status run_dkdv(const Shape& s, const void* q, const void* k, const void* v, 
 }
 
 // The two stages of the split backward: dK and dV (want_dq false) or dQ
-// (want_dq true), each recomputing P and dP; dense layouts, d in {64, 96, 128}.
+// (want_dq true), each recomputing P and dP; d in {64, 96, 128}; dense
+// layouts with a block mask or with dropout (not both), or packed layouts
+// without dropout.
 fa_status run_split(const Shape& s, bool want_dq, const void* q, const void* k, const void* v, const void* dO,
                     const float* lse, const float* delta, void* dq, void* dk, void* dv, const uint8_t* block_mask,
-                    int mask_heads, int causal, float scale, void* stream) {
+                    int mask_heads, int causal, float scale, void* stream, const fa::DropParams* drop = nullptr) {
   fa_status st = check_scale(scale);
   if (st != FA_OK) return st;
-  if (s.width() == 256) return FA_ERR_UNSUPPORTED;
+  const bool dropping = drop != nullptr && drop->t > 0;
+  if (s.width() == 256 || (dropping && (s.varlen() || block_mask))) return FA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) || !aligned16(delta))
     return FA_ERR_INVALID_ARG;
   if (want_dq ? !aligned16(dq) : (!aligned16(dk) || !aligned16(dv))) return FA_ERR_INVALID_ARG;
@@ -275,6 +278,8 @@ fa_status run_split(const Shape& s, bool want_dq, const void* q, const void* k, 
   a.scale_log2 = scale * kLog2e;
   a.block_mask = block_mask;
   a.mask_heads = mask_heads;
+  a.dropout = dropping;
+  if (dropping) a.drop = *drop;
   a.status = status_word();
   if (!a.status) return FA_ERR_CUDA;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -325,16 +330,19 @@ fa_status run_backward(const Shape& s, const void* q, const void* k, const void*
   float* dq_accum =
       reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)s.q_rows() * sizeof(float)));
   // d <= 128 without dropout (dense with or without a block mask, or packed)
-  // takes the split backward (dQ by its own kernel, no accumulator); the rest
-  // accumulates dQ in the dK / dV kernel.
-  const bool split = !(drop && drop->t > 0) && s.width() != 256;
+  // takes the split backward (dQ by its own kernel, no accumulator); d = 256
+  // and dropout accumulate dQ in the dK / dV kernel.  With dropout the split
+  // kernels would each draw the keep mask again on their softmax warps'
+  // critical path (C4, p = 0.1: 2.90 + 1.66 ms against 3.51 ms for the
+  // accumulating kernel, whose otherwise idle dQ-drain warps draw it once).
+  const bool split = s.width() != 256 && !(drop && drop->t > 0);
   if (split) {
     if ((st = run_preprocess(s, o, dO, delta, nullptr, stream)) != FA_OK) return st;
     if ((st = run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, block_mask, mask_heads, causal, scale,
-                        stream)) != FA_OK)
+                        stream, drop)) != FA_OK)
       return st;
     return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, block_mask, mask_heads, causal, scale,
-                     stream);
+                     stream, drop);
   }
   if ((st = run_preprocess(s, o, dO, delta, dq_accum, stream)) != FA_OK) return st;
   if ((st = run_dkdv(s, q, k, v, dO, lse, delta, dq_accum, dk, dv, block_mask, mask_heads, causal, scale, stream,
@@ -597,6 +605,29 @@ fa_status fa_backward_dq_blocksparse(const void* q, const void* k, const void* v
   if ((st = check_block_mask(block_mask, mask_heads, B, H)) != FA_OK) return st;
   return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, block_mask, mask_heads, causal, scale,
                    stream);
+}
+
+fa_status fa_backward_dk_dv_dropout(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                    const float* delta, void* dk, void* dv, int B, int H, int N, int d, int dtype,
+                                    int causal, float scale, float p_drop, uint64_t seed, uint32_t offset,
+                                    void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return run_split(s, false, q, k, v, dO, lse, delta, nullptr, dk, dv, nullptr, 1, causal, scale, stream, &dp);
+}
+
+fa_status fa_backward_dq_dropout(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                 const float* delta, void* dq, int B, int H, int N, int d, int dtype, int causal,
+                                 float scale, float p_drop, uint64_t seed, uint32_t offset, void* stream) {
+  Shape s;
+  const fa_status st = dense_shape(B, H, N, N, d, dtype, &s);
+  if (st != FA_OK) return st;
+  fa::DropParams dp;
+  if (!make_drop(p_drop, seed, offset, &dp)) return FA_ERR_INVALID_ARG;
+  return run_split(s, true, q, k, v, dO, lse, delta, dq, nullptr, nullptr, nullptr, 1, causal, scale, stream, &dp);
 }
 
 fa_status fa_backward_dq_convert(const float* dq_accum, void* dq, int B, int H, int N, int d, int dtype,

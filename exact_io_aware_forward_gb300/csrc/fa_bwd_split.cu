@@ -95,15 +95,15 @@ struct DkdvSplitCfg : SplitCfg<D> {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     fa_bwd_dkdv_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                              const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                              void* __restrict__ dk, void* __restrict__ dv, const float* __restrict__ lse,
                              const float* __restrict__ delta, SeqLayout lay, int BH, int dh, float scale,
-                             float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads, int group,
-                             unsigned int* status) {
+                             float scale_log2, const uint8_t* __restrict__ block_mask, int mask_heads,
+                             DropParams drop, int group, unsigned int* status) {
   using C = DkdvSplitCfg<D>;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
@@ -362,6 +362,10 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
     for (int it = 0; it < n_it; ++it) {
       const int i = SPARSE ? i_sp : i_begin + it;
       const int q0 = i * C::BQ;
+      // Dropout: keep bits of this thread's key for the warpgroup's QW query
+      // columns (bit c <-> column c), drawn while S^T(i) is computed.
+      uint32_t kw = 0u;
+      if constexpr (DROP) kw = key_keep_words(key, q0 + QW * h, QW, lane, bh, drop).x;
       // the staged values of the previous tile have been read by every warp of the warpgroup
       if (it > 0 && !(ok = warp_wait(&ld_empty[h], (it - 1) & 1, abort_flag, status))) break;
       if (r < QW) {
@@ -413,6 +417,10 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
           p[sc][c] = p0;
           p[sc][c + 1] = p1;
           pk[sc][e] = pack2(p0, p1, BF16);
+          if constexpr (DROP) {  // dV takes the kept entries (scaled by the keep scale when stored)
+            const uint32_t b = kw >> (col + c);
+            pk[sc][e] &= ((b & 1u) ? 0x0000ffffu : 0u) | ((b & 2u) ? 0xffff0000u : 0u);
+          }
         }
       }
       // the P^T buffer is free once dV(i-1) has read it
@@ -440,7 +448,16 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
         for (int e = 0; e < 8; ++e) {
           const int c = 2 * e;
           const float2 nd = *reinterpret_cast<const float2*>(sND + col + c);
-          const uint64_t t2 = f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(nd.x, nd.y));
+          // dropout: dS = P (Z c dP - D), Z the keep bit and c the keep scale
+          uint64_t t2;
+          if constexpr (DROP) {
+            const uint32_t b = kw >> (col + c);
+            t2 = f2_fma(f2_pack(dp[c], dp[c + 1]),
+                        f2_pack((b & 1u) ? drop.keep_scale : 0.f, (b & 2u) ? drop.keep_scale : 0.f),
+                        f2_pack(nd.x, nd.y));
+          } else {
+            t2 = f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(nd.x, nd.y));
+          }
           float d0, d1;
           f2_unpack(f2_mul(f2_pack(p[sc][c], p[sc][c + 1]), t2), d0, d1);
           dk[e] = pack2(d0, d1, BF16);
@@ -475,7 +492,7 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
         const int cols = min(64, dh - 64 * half);
         if (n_it > 0) {
           store_rows_from_tmem<64, BF16>(lane_base + (is_dk ? C::COL_DK : C::COL_DV) + 64 * half, dst, key < Nk,
-                                         is_dk ? scale : 1.f, cols);
+                                         is_dk ? scale : (DROP ? drop.keep_scale : 1.f), cols);
         } else if (key < Nk) {
           for (int q = 0; q < cols / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(DkdvSplitCfg<D>::THREADS, 1)
       uint8_t* stage = (is_dk ? sDO : sQ) + half * C::SLAB;
       if (ok && has_half)
         stage_rows_from_tmem<64, BF16>(lane_base + (is_dk ? C::COL_DK : C::COL_DV) + 64 * half, stage, r,
-                                       is_dk ? scale : 1.f, n_it == 0);
+                                       is_dk ? scale : (DROP ? drop.keep_scale : 1.f), n_it == 0);
       fence_async_smem();
       named_barrier_sync(1 + h, 128);
       if (r == 0 && ok && has_half && !*abort_flag && 64 * half < dh) {
@@ -533,13 +550,14 @@ struct DqCfg : SplitCfg<D> {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      void* __restrict__ dq, const float* __restrict__ lse, const float* __restrict__ delta,
                      SeqLayout lay, int BH, int n_qblocks, int dh, float scale, float scale_log2,
-                     const uint8_t* __restrict__ block_mask, int mask_heads, int group, unsigned int* status) {
+                     const uint8_t* __restrict__ block_mask, int mask_heads, DropParams drop, int group,
+                     unsigned int* status) {
   using C = DqCfg<D>;
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
@@ -776,6 +794,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const uint64_t nd2 = f2_pack(nd, nd);
     for (int jt = 0, j = next_tile(0); ok && jt < n; ++jt, j = next_tile(j + 1)) {
       const int kb = (SPARSE ? j : jt) * C::BKV + KW * h;  // first key of this warpgroup's columns
+      // Dropout: keep bits of this row for the warpgroup's KW key columns
+      // (pair i: bits i and 16 + i), drawn while S(j) is computed.
+      uint32_t kw[1] = {0u};
+      if constexpr (DROP) tile_keep_bits<1>(kw, kb, q, bh, drop.offset, drop.k0, drop.k1, drop.t);
       if (!(ok = warp_wait(s_full, jt & 1, abort_flag, status))) break;
       tc_fence_after();
       float p[NC][16];
@@ -826,8 +848,17 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           float d0, d1;
-          f2_unpack(f2_mul(f2_pack(p[sc][2 * e], p[sc][2 * e + 1]), f2_add(f2_pack(dp[2 * e], dp[2 * e + 1]), nd2)),
-                    d0, d1);
+          uint64_t t2;  // dP - D, or with dropout Z c dP - D (Z the keep bit, c the keep scale)
+          if constexpr (DROP) {
+            const int pi = 8 * sc + e;  // pair of keys kb + 2 pi, kb + 2 pi + 1
+            t2 = f2_fma(f2_pack(dp[2 * e], dp[2 * e + 1]),
+                        f2_pack(((kw[0] >> pi) & 1u) ? drop.keep_scale : 0.f,
+                                ((kw[0] >> (16 + pi)) & 1u) ? drop.keep_scale : 0.f),
+                        nd2);
+          } else {
+            t2 = f2_add(f2_pack(dp[2 * e], dp[2 * e + 1]), nd2);
+          }
+          f2_unpack(f2_mul(f2_pack(p[sc][2 * e], p[sc][2 * e + 1]), t2), d0, d1);
           pk[sc][e] = pack2(d0, d1, BF16);
         }
       }
@@ -887,10 +918,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN, bool DROP>
 cudaError_t launch_dkdv_split_t(const SplitArgs& a, cudaStream_t stream) {
   using C = DkdvSplitCfg<D>;
-  auto kern = fa_bwd_dkdv_split_kernel<D, CAUSAL, BF16, SPARSE, VARLEN>;
+  auto kern = fa_bwd_dkdv_split_kernel<D, CAUSAL, BF16, SPARSE, VARLEN, DROP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_kt = (a.lay.Nk + C::BKV - 1) / C::BKV;  // packed batches: of the longest sequence
@@ -901,14 +932,15 @@ cudaError_t launch_dkdv_split_t(const SplitArgs& a, cudaStream_t stream) {
   const int group = (int)std::max(1LL, std::min(16LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.tm_dk, a.tm_dv, a.dk,
                                                          a.dv, a.lse, a.delta, a.lay, a.BH, a.dh, a.scale,
-                                                         a.scale_log2, a.block_mask, a.mask_heads, group, a.status);
+                                                         a.scale_log2, a.block_mask, a.mask_heads, a.drop, group,
+                                                         a.status);
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN>
+template <int D, bool CAUSAL, bool BF16, bool SPARSE, bool VARLEN, bool DROP>
 cudaError_t launch_dq_t(const SplitArgs& a, cudaStream_t stream) {
   using C = DqCfg<D>;
-  auto kern = fa_bwd_dq_kernel<D, CAUSAL, BF16, SPARSE, VARLEN>;
+  auto kern = fa_bwd_dq_kernel<D, CAUSAL, BF16, SPARSE, VARLEN, DROP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblocks = (a.lay.Nq + C::BQ - 1) / C::BQ;  // packed batches: of the longest sequence
@@ -919,7 +951,7 @@ cudaError_t launch_dq_t(const SplitArgs& a, cudaStream_t stream) {
   const int group = (int)std::max(1LL, std::min(64LL, (64LL << 20) / (per_head > 0 ? per_head : 1)));
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.dq, a.lse, a.delta, a.lay,
                                                          a.BH, n_qblocks, a.dh, a.scale, a.scale_log2, a.block_mask,
-                                                         a.mask_heads, group, a.status);
+                                                         a.mask_heads, a.drop, group, a.status);
   return cudaGetLastError();
 }
 
@@ -928,9 +960,10 @@ cudaError_t launch_dq_t(const SplitArgs& a, cudaStream_t stream) {
 cudaError_t launch_backward_dkdv_split(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream) {
 #define FA_SPLIT_CASE(DD, CC, BB)                                                               \
   if (d == DD && causal == CC && bf16 == BB)                                                   \
-    return a.lay.cu_q   ? launch_dkdv_split_t<DD, CC, BB, false, true>(a, stream)               \
-           : a.block_mask ? launch_dkdv_split_t<DD, CC, BB, true, false>(a, stream)             \
-                          : launch_dkdv_split_t<DD, CC, BB, false, false>(a, stream);
+    return a.lay.cu_q   ? launch_dkdv_split_t<DD, CC, BB, false, true, false>(a, stream)        \
+           : a.block_mask ? launch_dkdv_split_t<DD, CC, BB, true, false, false>(a, stream)      \
+           : a.dropout    ? launch_dkdv_split_t<DD, CC, BB, false, false, true>(a, stream)      \
+                          : launch_dkdv_split_t<DD, CC, BB, false, false, false>(a, stream);
   FA_SPLIT_CASE(64, false, false)
   FA_SPLIT_CASE(64, false, true)
   FA_SPLIT_CASE(64, true, false)
@@ -946,9 +979,10 @@ cudaError_t launch_backward_dkdv_split(int d, bool causal, bool bf16, const Spli
 cudaError_t launch_backward_dq(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream) {
 #define FA_DQ_CASE(DD, CC, BB)                                                                   \
   if (d == DD && causal == CC && bf16 == BB)                                                   \
-    return a.lay.cu_q   ? launch_dq_t<DD, CC, BB, false, true>(a, stream)                       \
-           : a.block_mask ? launch_dq_t<DD, CC, BB, true, false>(a, stream)                     \
-                          : launch_dq_t<DD, CC, BB, false, false>(a, stream);
+    return a.lay.cu_q   ? launch_dq_t<DD, CC, BB, false, true, false>(a, stream)                \
+           : a.block_mask ? launch_dq_t<DD, CC, BB, true, false, false>(a, stream)              \
+           : a.dropout    ? launch_dq_t<DD, CC, BB, false, false, true>(a, stream)              \
+                          : launch_dq_t<DD, CC, BB, false, false, false>(a, stream);
   FA_DQ_CASE(64, false, false)
   FA_DQ_CASE(64, false, true)
   FA_DQ_CASE(64, true, false)

@@ -110,8 +110,9 @@ cudaError_t launch_backward_dkdv_varlen(int d, bool causal, bool bf16, const Bwd
 cudaError_t launch_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, const DropParams& drop,
                                      cudaStream_t stream);
 // The backward pass with dQ computed by a kernel of its own (dense layouts
-// with or without a block mask, packed variable-length batches; no dropout):
-// a dK / dV kernel and a dQ kernel that both recompute P and dP on chip.
+// with a block mask, with dropout or with neither; packed variable-length
+// batches without dropout): a dK / dV kernel and a dQ kernel that both
+// recompute P and dP on chip.
 struct SplitArgs {
   CUtensorMap tm_q, tm_do;         // box 64 columns x 128 rows
   CUtensorMap tm_k, tm_v;          // box 64 columns x 128 rows
@@ -126,6 +127,8 @@ struct SplitArgs {
   float scale, scale_log2;
   const uint8_t* block_mask = nullptr;  // as FwdArgs (128 x 128 blocks); null = dense
   int mask_heads = 1;
+  bool dropout = false;                 // apply `drop` (dense layouts only)
+  DropParams drop;
   unsigned int* status;
 };
 cudaError_t launch_backward_dkdv_split(int d, bool causal, bool bf16, const SplitArgs& a, cudaStream_t stream);

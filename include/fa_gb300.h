@@ -117,6 +117,8 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  *   - accumulated (d = 256, dropout): fa_backward_preprocess,
  *     fa_backward_dkdv, fa_backward_dq_convert -- dQ partials added into a
  *     float32 accumulator by the dK / dV kernel.
+ *     (fa_backward_dk_dv_dropout / fa_backward_dq_dropout run dropout on the
+ *     split kernels for callers without room for the accumulator.)
  * All stages run in order on `stream`.  `workspace` must hold
  * fa_backward_workspace_size(B,H,N,d) bytes (else FA_ERR_WORKSPACE); its
  * contents on entry do not matter and are overwritten.
@@ -167,6 +169,25 @@ fa_status fa_backward_dkdv_dropout(const void* q, const void* k, const void* v, 
                                    const float* delta, float* dq_accum, void* dk, void* dv, int B, int H, int N,
                                    int d, int dtype, int causal, float scale, float p_drop, uint64_t seed,
                                    uint32_t offset, void* stream);
+/*
+ * The split backward with dropout, d in {64, 96, 128}: no float32 dQ
+ * accumulator, at the price of drawing the keep mask in both kernels
+ * (fa_backward_dropout, which accumulates dQ, is faster).  With Z the
+ * regenerated keep mask and c = 256 / (256 - t),
+ *   dV = c (P * Z)^T dO,  dS = P * (c Z * (dO V^T) - D),  dK = s dS^T Q,
+ *   dQ = s dS K,
+ * D = rowsum(dO * O) from fa_backward_preprocess(o, dO, delta, NULL, ...).
+ * fa_backward_dk_dv_dropout writes dk, dv; fa_backward_dq_dropout writes dq
+ * (no workspace).  Dropout arguments as fa_forward_dropout, the rest as
+ * fa_backward_dk_dv / fa_backward_dq; d = 256 gives FA_ERR_UNSUPPORTED.
+ */
+fa_status fa_backward_dk_dv_dropout(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                    const float* delta, void* dk, void* dv, int B, int H, int N, int d, int dtype,
+                                    int causal, float scale, float p_drop, uint64_t seed, uint32_t offset,
+                                    void* stream);
+fa_status fa_backward_dq_dropout(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                                 const float* delta, void* dq, int B, int H, int N, int d, int dtype, int causal,
+                                 float scale, float p_drop, uint64_t seed, uint32_t offset, void* stream);
 
 /*
  * The keep mask the dropout entry points use, written out: keep is a device

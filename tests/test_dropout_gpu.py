@@ -121,6 +121,10 @@ def test_dropout_zero_is_plain_attention():
 
 
 def test_dropout_stages_equal_the_full_call():
+    """fa_backward_dropout accumulates dQ: preprocess + fa_backward_dkdv_dropout
+    + dq_convert give its result bit for bit.  The split stages
+    (fa_backward_dk_dv_dropout + fa_backward_dq_dropout, no accumulator) agree
+    within the 16-bit rounding of the two orders."""
     B, H, N, d = 1, 3, 700, 128
     dev = torch.device("cuda:0")
     q, k, v, do = (x.to(dev) for x in attention_inputs(B, H, N, d, "bf16", seed=63))
@@ -139,3 +143,40 @@ def test_dropout_stages_equal_the_full_call():
     fa.fa_device_status()
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
     assert float((dq.float() - dq2.float()).abs().max()) <= 1e-2 * float(dq.float().abs().max())
+    dq3, dk3, dv3 = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    fa.fa_backward_dk_dv_dropout(q, k, v, do, lse, delta, dk3, dv3, p, seed, offset)
+    fa.fa_backward_dq_dropout(q, k, v, do, lse, delta, dq3, p, seed, offset)
+    fa.fa_device_status()
+    for x, y in ((dq, dq3), (dk, dk3), (dv, dv3)):
+        assert float((x.float() - y.float()).abs().max()) <= 1e-2 * float(x.float().abs().max())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d,dtype,p", [(650, 64, "fp16", 0.2), (300, 96, "bf16", 0.5)])
+def test_dropout_split_stages_match_oracle(causal, N, d, dtype, p):
+    """The split stages alone against the oracle on ragged sizes (B = 2, so the
+    head index b * H + h of the generator's counter is exercised)."""
+    B, H = 2, 2
+    dev = torch.device("cuda:0")
+    q, k, v, do = attention_inputs(B, H, N, d, dtype, seed=6100 + N + causal)
+    seed, offset = 2**33 + 17, 9
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, causal=causal, dropout_p=p, seed=seed, offset=offset)
+    delta = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+    fa.fa_backward_preprocess(o, dod, delta, None)
+    fa.fa_backward_dk_dv_dropout(qd, kd, vd, dod, lse, delta, dk, dv, p, seed, offset, causal=causal)
+    fa.fa_backward_dq_dropout(qd, kd, vd, dod, lse, delta, dq, p, seed, offset, causal=causal)
+    fa.fa_device_status()
+    out = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
+    _check(q, k, v, do, causal, p, seed, offset, *out, dtype)
+
+
+def test_dropout_split_stages_reject_d256():
+    B, H, N, d = 1, 1, 128, 256
+    dev = torch.device("cuda:0")
+    q, k, v, do = (x.to(dev) for x in attention_inputs(B, H, N, d, "bf16", seed=64))
+    lse = torch.zeros((B, H, N), device=dev, dtype=torch.float32)
+    delta = torch.zeros_like(lse)
+    with pytest.raises(fa.FAError):
+        fa.fa_backward_dq_dropout(q, k, v, do, lse, delta, torch.empty_like(q), 0.1, 1, 0)
