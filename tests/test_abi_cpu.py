@@ -127,7 +127,20 @@ def test_dropout_validation(lib):
         rc = lib.fa_backward_dkdv_dropout(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125, p,
                                           1, 0, None)
         assert rc == 1, p
+        rc = lib.fa_backward_dk_dv_dropout(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125, p, 1, 0,
+                                           None)
+        assert rc == 1, p
+        rc = lib.fa_backward_dq_dropout(ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125, p, 1, 0, None)
+        assert rc == 1, p
         assert lib.fa_dropout_keep_mask(ptr, 1, 4, 4, p, 1, 0, None) == 1
+    # the split dropout stages: d = 256 is unsupported, a misaligned tensor is
+    # an invalid argument, both before any launch
+    assert lib.fa_backward_dq_dropout(ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 256, 1, 0, 0.0625, 0.1, 1, 0,
+                                      None) == 2
+    assert lib.fa_backward_dk_dv_dropout(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 256, 1, 0, 0.0625, 0.1, 1,
+                                         0, None) == 2
+    assert lib.fa_backward_dq_dropout(ptr + 2, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 16, 64, 1, 0, 0.125, 0.1, 1, 0,
+                                      None) == 1
     assert lib.fa_dropout_keep_mask(None, 1, 4, 4, 0.5, 1, 0, None) == 1
     assert lib.fa_dropout_keep_mask(ptr, 0, 4, 4, 0.5, 1, 0, None) == 1
 
