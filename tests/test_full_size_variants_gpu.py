@@ -1,0 +1,167 @@
+"""Parity of the variant workloads at the sizes and launch configurations the
+benchmark times: block-sparse S1, C4 with dropout, packed batch V1, d = 256
+(W256) and d = 96 (W96).
+
+Each runs through the public API exactly as the benchmark's lines do; the
+float64 oracle then checks every gradient of two whole heads (or sequences)
+and O / LSE on tile-edge and random rows of every head, and invariants that
+hold at any size (P rows sum to 1: sum_j dK_j = 0, sum_j dV_j = sum_i dO_i).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_forward_gb300 as fa
+from exact_io_aware_forward_gb300.synth import (S1, V1, W96, W256, WORKLOADS, as_float64, blocksparse_inputs,
+                                                varlen_workload_inputs, workload_inputs)
+from oracle import attention as A
+from oracle import dropout as DR
+
+from gpu_util import GRAD_REL_FRO, LSE_TOL, O_TOL, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+# The dropout configuration of the benchmark's dropout line.
+DROP_P, DROP_SEED, DROP_OFFSET = 0.1, 2024, 0
+
+
+def _rows(N, rng, n=12):
+    return np.unique(np.concatenate([[0, 1, 127, 128, N // 2, N - 1], rng.integers(0, N, n)]))
+
+
+def _check_head_grads(got, want):
+    for name, g, r in zip(("dq", "dk", "dv"), got, want):
+        e = rel_fro(g, r)
+        assert e <= GRAD_REL_FRO, (name, e)
+
+
+def _invariants(dk, dv, do):
+    """Per head: sum over keys of dK is 0 and of dV is sum over queries of dO
+    (every query row sees at least one key in these workloads)."""
+    dkf = dk.float().sum(dim=-2)
+    assert float(dkf.abs().max()) <= 1e-2 * float(dk.float().abs().sum(dim=-2).max())
+    dvs, dos = dv.float().sum(dim=-2), do.float().sum(dim=-2)
+    assert float((dvs - dos).abs().max()) <= 1e-2 * float(dos.abs().max() + 1)
+
+
+def test_blocksparse_s1_full_size():
+    w = S1
+    q, k, v, do, bm = blocksparse_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    md = torch.from_numpy(bm.astype(np.uint8)).to(dev)
+    o, lse = fa.forward(qd, kd, vd, causal=w.causal, block_mask=md)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=w.causal, block_mask=md)
+    fa.fa_device_status()
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    qf, kf, vf, dof = as_float64(q, k, v, do)
+    s = 1.0 / math.sqrt(w.d)
+    rng = np.random.default_rng(11)
+    mask_of = lambda b, h: bm[0 if bm.shape[0] == 1 else b * w.H + h]  # noqa: E731
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        want = A.backward_head(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, w.causal, block_mask=mask_of(b, h))
+        _check_head_grads([x[b, h].double().numpy() for x in (dq, dk, dv)], want)
+    for b in range(w.B):
+        for h in range(w.H):
+            r = _rows(w.N, rng, 4)
+            ro, rl = A.forward_head(qf[b, h], kf[b, h], vf[b, h], s, w.causal, rows=r, block_mask=mask_of(b, h))
+            assert float(np.abs(o[b, h].double().numpy()[r] - ro).max()) <= O_TOL[w.dtype], (b, h)
+            assert float(np.abs(lse[b, h].double().numpy()[r] - rl).max()) <= LSE_TOL, (b, h)
+    _invariants(dk, dv, do)
+
+
+def test_dropout_c4_full_size():
+    w = WORKLOADS["C4"]
+    q, k, v, do = workload_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, causal=w.causal, dropout_p=DROP_P, seed=DROP_SEED, offset=DROP_OFFSET)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=w.causal, dropout_p=DROP_P, seed=DROP_SEED,
+                             offset=DROP_OFFSET)
+    fa.fa_device_status()
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    qf, kf, vf, dof = as_float64(q, k, v, do)
+    s = 1.0 / math.sqrt(w.d)
+    c = DR.keep_scale(DROP_P)
+    rng = np.random.default_rng(12)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        bh = b * w.H + h
+        keep = DR.keep_mask(DROP_SEED, DROP_OFFSET, DROP_P, bh, w.N, w.N)
+        want = A.backward_head(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, w.causal, keep=keep, keep_scale=c)
+        _check_head_grads([x[b, h].double().numpy() for x in (dq, dk, dv)], want)
+        r = _rows(w.N, rng, 58)
+        ro, rl = A.forward_head(qf[b, h], kf[b, h], vf[b, h], s, w.causal, rows=r, keep=keep[r], keep_scale=c)
+        # kept weights are scaled by 1/(1-p): the 16-bit floor is one ulp at the largest |O|
+        tol = max(O_TOL[w.dtype], 2.0 ** -8 * float(np.abs(ro).max()))
+        assert float(np.abs(o[b, h].double().numpy()[r] - ro).max()) <= tol, (b, h)
+        assert float(np.abs(lse[b, h].double().numpy()[r] - rl).max()) <= LSE_TOL, (b, h)
+    # LSE does not depend on the mask: every head against the plain oracle on a few rows
+    for b in range(w.B):
+        for h in range(w.H):
+            r = _rows(w.N, rng, 2)
+            _, rl = A.forward_head(qf[b, h], kf[b, h], vf[b, h], s, w.causal, rows=r)
+            assert float(np.abs(lse[b, h].double().numpy()[r] - rl).max()) <= LSE_TOL, (b, h)
+
+
+def test_varlen_v1_full_size():
+    w = V1
+    q, k, v, do, cu_q, cu_k = varlen_workload_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    cqd, ckd = cu_q.to(dev), cu_k.to(dev)
+    mx = max(w.lengths)
+    o, lse = fa.forward_varlen(qd, kd, vd, cqd, ckd, mx, mx, causal=w.causal)
+    dq, dk, dv = fa.backward_varlen(qd, kd, vd, o, lse, dod, cqd, ckd, mx, mx, causal=w.causal)
+    fa.fa_device_status()
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    s = 1.0 / math.sqrt(w.d)
+    cq = cu_q.numpy()
+    lengths = np.asarray(w.lengths)
+    seqs = sorted({int(np.argmax(lengths)), int(np.argmin(lengths)), len(lengths) // 2})
+    for sq in seqs:
+        a, e = int(cq[sq]), int(cq[sq + 1])
+        for h in (0, w.H - 1):
+            qs, ks, vs, dos = (x[a:e, h].double().numpy() for x in (q, k, v, do))
+            ro, rl = A.forward_head(qs, ks, vs, s, w.causal)
+            assert float(np.abs(o[a:e, h].double().numpy() - ro).max()) <= O_TOL[w.dtype], (sq, h)
+            assert float(np.abs(lse[a:e, h].double().numpy() - rl).max()) <= LSE_TOL, (sq, h)
+            want = A.backward_head(qs, ks, vs, dos, s, w.causal)
+            _check_head_grads([x[a:e, h].double().numpy() for x in (dq, dk, dv)], want)
+    # invariants per sequence and head
+    for sq in range(len(lengths)):
+        a, e = int(cq[sq]), int(cq[sq + 1])
+        _invariants(dk[a:e].transpose(0, 1), dv[a:e].transpose(0, 1), do[a:e].transpose(0, 1))
+
+
+@pytest.mark.parametrize("name", ["W256", "W96"])
+def test_head_dim_workloads_full_size(name):
+    w = {"W256": W256, "W96": W96}[name]
+    q, k, v, do = workload_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, causal=w.causal)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=w.causal)
+    fa.fa_device_status()
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    qf, kf, vf, dof = as_float64(q, k, v, do)
+    s = 1.0 / math.sqrt(w.d)
+    rng = np.random.default_rng(13)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        want = A.backward_head(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, w.causal)
+        _check_head_grads([x[b, h].double().numpy() for x in (dq, dk, dv)], want)
+    for b in range(w.B):
+        for h in range(w.H):
+            r = _rows(w.N, rng, 4)
+            ro, rl = A.forward_head(qf[b, h], kf[b, h], vf[b, h], s, w.causal, rows=r)
+            assert float(np.abs(o[b, h].double().numpy()[r] - ro).max()) <= O_TOL[w.dtype], (b, h)
+            assert float(np.abs(lse[b, h].double().numpy()[r] - rl).max()) <= LSE_TOL, (b, h)
+            # dQ of a causal row with fewer than 16 visible keys is a difference of nearly
+            # equal terms that 16-bit P and dS round by up to a few percent of its small
+            # norm (row 1: two keys); those rows are covered by the whole-head checks
+            # above, whose relative error is 0.24% here (the 16-bit floor of dQ: 0.17%).
+            r = r[(r == 0) | (r >= 16)]
+            ref = A.backward_head_rows(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, w.causal, r)
+            assert rel_fro(dq[b, h].double().numpy()[r], ref) <= GRAD_REL_FRO, (b, h)
+    _invariants(dk, dv, do)
