@@ -1,7 +1,9 @@
 // Forward pass: launch dispatch for dense layouts without dropout.  Block
 // masks run the kernel in fa_fwd_kernel.cuh; plain dense attention runs the
 // kernel of fa_fwd_persist.cu (Q with a producer of its own, per-query-tile
-// O hand-off, persistent CTAs at d = 64).
+// O hand-off, persistent CTAs at d = 64), except non-causal attention at
+// d = 128, where the kernel of fa_fwd_kernel.cuh measured faster (N = 32768:
+// 3.21 against 3.28 ms; causal C4: 0.898 against 0.877 ms the other way).
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -9,8 +11,9 @@ namespace {
 
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_fwd_s(const FwdArgs& a, cudaStream_t stream) {
-  return a.block_mask ? launch_fwd_t<D, CAUSAL, BF16, true, false, false>(a, stream)
-                      : launch_forward_persistent(D, CAUSAL, BF16, a, stream);
+  if (a.block_mask) return launch_fwd_t<D, CAUSAL, BF16, true, false, false>(a, stream);
+  if constexpr (D == 128 && !CAUSAL) return launch_fwd_t<D, CAUSAL, BF16, false, false, false>(a, stream);
+  return launch_forward_persistent(D, CAUSAL, BF16, a, stream);
 }
 
 }  // namespace
