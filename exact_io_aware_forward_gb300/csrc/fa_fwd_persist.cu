@@ -10,17 +10,18 @@
 //   - O_t has its own full / empty barriers per query tile: softmax
 //     warpgroup 0 (one key tile fewer under the causal mask) writes its O
 //     rows while warpgroup 1 finishes the item;
-//   - at d = 64 CTAs are persistent (kPersistent): the grid has one CTA per
+//   - at d = 64, and at d = 128 with short keys, CTAs are persistent: the grid has one CTA per
 //     work item (a head and 256 query rows, heads in L2 groups, heaviest
 //     query blocks first), but a running CTA, a few key tiles before the end
 //     of its item, cancels through cluster launch control the launch of a
 //     CTA that has not started and does that CTA's item itself.  TMEM,
 //     barriers and descriptors are then set up once per SM, the K / V ring
 //     flows on into the next item, and the next item's Q is pulled into L2
-//     and loaded while the current item ends.  At d = 128 one CTA per item
-//     measured faster (the cancellation answers come back only roughly in
-//     grid order, and the chained items' running phase bases cost the
-//     single MMA-issuing thread instructions).
+//     and loaded while the current item ends.  At d = 128 with long keys
+//     one CTA per item measured faster (the cancellation answers come back
+//     only roughly in grid order, and the chained items' running phase bases
+//     cost the single MMA-issuing thread instructions, which items of many
+//     key tiles do not win back).
 // The MMA issuer's loop per item is the one-shot kernel's: PV_0(j-1), S_0(j),
 // PV_1(j-1), S_1(j) from one thread.
 //
@@ -63,11 +64,14 @@ struct PersistCfg {
   static constexpr uint32_t NEXT_READERS = 10;
 };
 
-// Whether CTAs take further items (measured per head dimension: at d = 64 a
-// CTA that stays resident was 2-4% faster than one CTA per item, at d = 128
-// 1-6% slower, with the same code otherwise).
+// Whether CTAs take further items, measured with the same code otherwise: at
+// d = 64 a CTA that stays resident was 2-4% faster than one CTA per item (N =
+// 4096); at d = 128 causal it is faster for short keys (N = 1024: 9%, 2048:
+// 3.6%) and slower for long ones (4096: 1%, 8192: 4%), where items are long
+// enough to amortise their start and the claimed items' order costs more.
 template <int D>
-constexpr bool kPersistent = D == 64;
+constexpr bool kAlwaysPersistent = D == 64;
+constexpr int kPersistMaxKeys = 2048;  // d = 128: persistent up to this many keys
 
 // The K / V producer asks for the next item when it starts loading the
 // kClaimAhead-th last key tile of the current one (it runs NS / 2 key tiles
@@ -443,10 +447,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16>
-cudaError_t launch_persist_t(const FwdArgs& a, cudaStream_t stream) {
+template <int D, bool CAUSAL, bool BF16, bool PERSIST>
+cudaError_t launch_persist_k(const FwdArgs& a, cudaStream_t stream) {
   using C = PersistCfg<D>;
-  auto kern = fa_fwd_persist_kernel<D, CAUSAL, BF16, kPersistent<D>>;
+  auto kern = fa_fwd_persist_kernel<D, CAUSAL, BF16, PERSIST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int n_qblocks = (a.lay.Nq + C::QT * C::BM - 1) / (C::QT * C::BM);
@@ -458,6 +462,16 @@ cudaError_t launch_persist_t(const FwdArgs& a, cudaStream_t stream) {
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.lay, a.BH, n_qblocks,
                                                          a.scale_log2, group, a.status);
   return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_persist_t(const FwdArgs& a, cudaStream_t stream) {
+  if constexpr (kAlwaysPersistent<D>) {
+    return launch_persist_k<D, CAUSAL, BF16, true>(a, stream);
+  } else {
+    return a.lay.Nk <= kPersistMaxKeys ? launch_persist_k<D, CAUSAL, BF16, true>(a, stream)
+                                       : launch_persist_k<D, CAUSAL, BF16, false>(a, stream);
+  }
 }
 
 }  // namespace
