@@ -90,3 +90,19 @@ def test_forward_full_size_sampled_rows(name):
             eo, el = check_forward_heads(q, k, v, o, lse, w.causal, heads=[(b, h)], rows=few)
             assert eo <= O_TOL[w.dtype] and el <= LSE_TOL, (b, h, eo, el)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [2047, 2048, 2049, 3000])
+def test_forward_d128_around_the_persistence_threshold(N, causal):
+    """d = 128 dense attention is dispatched by key length and mask: causal
+    runs persistent CTAs up to 2048 keys and one CTA per item above, non-causal
+    runs the one-shot kernel.  Every head of B = 2, H = 5 (a partial L2 head
+    group) on tile-edge and random rows."""
+    B, H, d = 2, 5, 128
+    q, k, v, _ = attention_inputs(B, H, N, d, "bf16", seed=900 + N + causal, with_do=False)
+    o, lse = gpu_forward(q, k, v, causal)
+    rng = np.random.default_rng(N)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, N - 2, N - 1], rng.integers(0, N, 24)]))
+    eo, el = check_forward_heads(q, k, v, o, lse, causal, rows=rows)
+    assert eo <= O_TOL["bf16"] and el <= LSE_TOL, (eo, el)
