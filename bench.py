@@ -37,6 +37,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 DKDV_PROFILE = os.path.join(ROOT, "profiles", "fa_bwd_dkdv_split_C4_causal_n8192_d128_bf16.md")
 DKDV_SOURCES = ("fa_bwd_split.cu", "fa_bwd_kernel.cuh", "fa_ptx.cuh", "fa_internal.h", "fa_layout.cuh",
                 "fa_philox.cuh")
+# The same for the variant lines whose roofline object is the split dK/dV kernel.
+VARIANT_PROFILES = {
+    "blocksparse": os.path.join(ROOT, "profiles", "fa_bwd_dkdv_split_blocksparse_S1_n8192_d128_bf16.md"),
+    "varlen": os.path.join(ROOT, "profiles", "fa_bwd_dkdv_split_varlen_V1_causal_d128_bf16.md"),
+}
 
 
 def kernel_source_hash(names=DKDV_SOURCES) -> str:
@@ -597,6 +602,11 @@ def run_variant(args, world, rank, local, kind):
         alg = "10*N^2*d per head (5 GEMMs), halved causal, per launch"
         h2d_extra = 0
         what = "with the keep mask drawn by the oracle's generator"
+    # DRAM traffic of the roofline kernel from the committed capture of this very workload, if any
+    from exact_io_aware_forward_gb300.synth import S1, V1
+    traffic, traffic_src = None, "no capture"
+    if (kind, w.name) in (("blocksparse", S1.name), ("varlen", V1.name)):
+        traffic, traffic_src = captured_traffic(VARIANT_PROFILES[kind])
     return {
         "metric": metric, "value": round(world * value, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -613,7 +623,8 @@ def run_variant(args, world, rank, local, kind):
                        "bwd_dkdv": round(parts[2], 4), "bwd_dq_convert": round(parts[3], 4)}),
         "roofline": {"bound": "tensor", "kernel": kern,
                      "achieved": round(dkdv, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(dkdv / peak, 4),
-                     "traffic": None, "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic": alg},
+                     "traffic": traffic, "traffic_source": traffic_src,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic": alg},
         "e2e": {"value": round(world * 2.5 * F / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(4 * elem + h2d_extra),
                 "d2h_bytes_per_step": int(4 * elem + hlse.numel() * 4), "ms_per_step": round(e2e_ms, 3)},

@@ -160,3 +160,12 @@ def test_fma_pipe_exp2_error_bound():
     assert np.abs(_exp2_poly_f32(ints) / np.exp2(ints) - 1).max() < 1e-4
     low = _exp2_poly_f32(np.array([-np.inf, -1e30, -200.0]))
     assert np.all(low > 0) and np.all(low < 3e-38)
+
+
+def test_committed_dkdv_profiles_carry_traffic_and_hash():
+    """Every profile the bench lines read records a traffic figure and a source hash."""
+    import re
+    for path in (bench.DKDV_PROFILE, *bench.VARIANT_PROFILES.values()):
+        text = open(path, encoding="utf-8").read()
+        assert re.search(r"^traffic_bytes_per_launch: \d+$", text, re.M), path
+        assert re.search(r"^source_sha256_16: `[0-9a-f]{16}`$", text, re.M), path
