@@ -295,7 +295,7 @@ def run_decode(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) Q, K, V; no dataset)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
                    "l2": "flushed (256 MB write) before every timed call"},
-        "roofline": {"bound": "hbm", "kernel": "fa_decode_split_kernel + fa_decode_combine_kernel",
+        "roofline": {"bound": "hbm", "kernel": "fa_decode_tc_kernel + fa_decode_combine_kernel",
                      "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
                      "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic": "K + V + Q + O bytes per call"},

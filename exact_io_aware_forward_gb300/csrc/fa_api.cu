@@ -660,9 +660,7 @@ fa_status decode_plan(int B, int H, int Nq, int Nk, int d, int num_splits, int* 
   const long long BH = (long long)B * H;
   if (BH > 65535 || BH * Nk * d >= (1LL << 31) || BH * Nq * d >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > 1024) return FA_ERR_INVALID_ARG;
-  int s = num_splits ? num_splits
-                     : fa::decode_uses_tc(Nq, d) ? fa::decode_tc_default_splits((int)BH, Nq, Nk)
-                                                 : fa::decode_default_splits((int)BH, Nq, Nk);
+  int s = num_splits ? num_splits : fa::decode_default_splits((int)BH, Nq, Nk);
   const int c = fa::decode_chunk(Nk, s);
   s = (Nk + c - 1) / c;  // no empty trailing chunk
   const size_t rows = (size_t)s * BH * Nq;
@@ -697,9 +695,6 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FA_ERR_WORKSPACE;
   fa::DecodeArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
   a.o = o;
   a.lse = lse;
   a.BH = B * H;
@@ -713,19 +708,15 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o
   a.o_part = static_cast<float*>(workspace);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)));
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (fa::decode_uses_tc(Nq, d)) {  // several queries per head: the tensor-core split kernel
-    Shape sh;
-    if (dense_shape(B, H, Nq, Nk, d, dtype, &sh) != FA_OK) return FA_ERR_INVALID_ARG;
-    if (!make_map(&a.tm_q, q, sh, false, 128) || !make_map(&a.tm_k, k, sh, true, 128) ||
-        !make_map(&a.tm_v, v, sh, true, 128))
-      return FA_ERR_CUDA;
-    a.status = status_word();
-    if (!a.status) return FA_ERR_CUDA;
-    if (fa::launch_decode_tc(d, dtype == FA_BF16, a, cs) != cudaSuccess) return FA_ERR_CUDA;
-    return fa::launch_decode_combine(d, dtype == FA_BF16, a, cs) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-  }
-  if (fa::launch_decode(d, dtype == FA_BF16, a, cs) != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
+  Shape sh;
+  if (dense_shape(B, H, Nq, Nk, d, dtype, &sh) != FA_OK) return FA_ERR_INVALID_ARG;
+  if (!make_map(&a.tm_q, q, sh, false, 128) || !make_map(&a.tm_k, k, sh, true, 128) ||
+      !make_map(&a.tm_v, v, sh, true, 128))
+    return FA_ERR_CUDA;
+  a.status = status_word();
+  if (!a.status) return FA_ERR_CUDA;
+  if (fa::launch_decode_tc(d, dtype == FA_BF16, a, cs) != cudaSuccess) return FA_ERR_CUDA;
+  return fa::launch_decode_combine(d, dtype == FA_BF16, a, cs) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_selftest_wait_timeout(void* stream) {

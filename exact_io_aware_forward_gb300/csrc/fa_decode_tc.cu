@@ -1,10 +1,10 @@
 // Split-KV forward on the tensor cores for decoding (few queries against many
-// keys), d in {64, 128}: from one query per head up to several (speculative
-// or chunked decoding), 128 queries per CTA.
+// keys), d in {64, 128, 256}: from one query per head up to several
+// (speculative or chunked decoding, grouped-query heads), 128 queries per CTA.
 //
-// The key range of every head is cut into contiguous chunks (as for the
-// CUDA-core kernel in fa_decode.cu, whose workspace layout and combine kernel
-// this one shares); a CTA takes up to 128 queries of one head against one
+// The key range of every head is cut into contiguous chunks (the plan and the
+// combine kernel that merges the chunks are in fa_decode.cu); a CTA takes up
+// to 128 queries of one head against one
 // chunk, so each K and V tile is read from memory once for all of them,
 // and evaluates the online-softmax recurrence ("FlashAttention 为什么不需要存下
 // 注意力矩阵", jefxiong.cn, section 3.2) over the chunk's 128-key tiles:
@@ -17,6 +17,10 @@
 // Roles (256 threads): warp 0 TMA (Q once; K / V tiles in consumption order
 // through a ring), warp 1 TMEM allocation and the MMA issuer, warps 4-7 the
 // softmax (one query row per thread), then the chunk's epilogue.
+// d = 256: O takes 256 TMEM columns (S_a 128 | S_b 128 | O 256), a K or V
+// tile 64 KB, so K and V move through the ring in 128-feature halves (five
+// 32 KB slots beside the 64 KB Q tile); S(j) runs over both halves of K_j
+// (16 K-steps) and PV(j) is two N = 128 products, one per half of V_j and O.
 // Causal (queries are the last Nq of Nk positions): key j is visible to
 // query i iff j <= i + Nk - Nq; tiles past the query tile's last visible key
 // are not read, a chunk no query of the tile sees writes LSE_s = -inf.
@@ -31,11 +35,15 @@ struct DecTcCfg {
   static constexpr int BN = 128;                   // keys per tile
   static constexpr int SLABS = D / 64;
   static constexpr int SLAB = 128 * 128;           // 128 rows x 64 columns x 16 bit
-  static constexpr int TILE = SLABS * SLAB;
-  static constexpr int NS = D == 128 ? 4 : 8;      // ring slots
+  static constexpr int TILE = SLABS * SLAB;        // the Q tile
+  static constexpr bool HALVES = D == 256;         // K / V in 128-feature halves
+  static constexpr int PER = HALVES ? 2 : 1;       // ring items per K or V tile
+  static constexpr int ITEM_SLABS = SLABS / PER;
+  static constexpr int ITEM = ITEM_SLABS * SLAB;   // one ring slot
+  static constexpr int NS = D == 256 ? 5 : (D == 128 ? 4 : 8);  // ring slots
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = TILE;
-  static constexpr int OFF_BAR = OFF_RING + NS * TILE;
+  static constexpr int OFF_BAR = OFF_RING + NS * ITEM;
   // q_full, ring_full[NS], ring_empty[NS], s_full[2], p_full[2], pv_done[2], o_full, drain
   static constexpr int NBAR = 1 + 2 * NS + 6 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_items = 2 * n;
+  const int n_items = 2 * n * C::PER;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -149,11 +157,12 @@ __global__ void __launch_bounds__(256, 1)
         if (!mbar_wait(&ring_empty[slot], ((p / C::NS) & 1) ^ 1, abort_flag, status, kStatusTimeout)) break;
         bool is_v;
         int t;
-        dec_ring_item(p, n, is_v, t);
-        mbar_arrive_expect_tx(&ring_full[slot], C::TILE);
-        for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sRing + slot * C::TILE + s * C::SLAB, is_v ? &tm_v : &tm_k, &ring_full[slot], s * 64,
-                      kb + t * C::BN, bh);
+        dec_ring_item(p / C::PER, n, is_v, t);
+        const int half = p % C::PER;
+        mbar_arrive_expect_tx(&ring_full[slot], C::ITEM);
+        for (int s = 0; s < C::ITEM_SLABS; ++s)
+          tma_load_3d(sRing + slot * C::ITEM + s * C::SLAB, is_v ? &tm_v : &tm_k, &ring_full[slot],
+                      (half * C::ITEM_SLABS + s) * 64, kb + t * C::BN, bh);
         issued = p + 1;
       }
       if (*abort_flag) {
@@ -166,7 +175,7 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(128, C::BN, BF16, false, false);
-      constexpr uint32_t kIdPV = idesc_f16(128, D, BF16, false, true);
+      constexpr uint32_t kIdPV = idesc_f16(128, D / C::PER, BF16, false, true);
       const uint32_t aq = smem_u32(sQ), ring = smem_u32(sRing);
       int p = 0;  // ring position of the next item
       auto take = [&](int& slot) {
@@ -175,43 +184,47 @@ __global__ void __launch_bounds__(256, 1)
         ++p;
         return ok;
       };
-      auto issue_s = [&](int b, int slot) {
+      // takes the ring slots of the next K or V tile (PER items)
+      auto take_tile = [&](int (&sl)[C::PER]) {
+        for (int h = 0; h < C::PER; ++h)
+          if (!take(sl[h])) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto issue_s = [&](int b, const int (&sl)[C::PER]) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * C::SLAB + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S + 128 * b, sdesc_sw128(aq + o, 16, 1024),
-                 sdesc_sw128(ring + slot * C::TILE + o, 16, 1024), kIdS, kk > 0);
+          const int h = kk / (D / 16 / C::PER);  // the K slot holding K-step kk
+          const int kl = kk % (D / 16 / C::PER);
+          const uint32_t oa = (kk >> 2) * C::SLAB + (kk & 3) * 32;
+          const uint32_t ob = (kl >> 2) * C::SLAB + (kl & 3) * 32;
+          mma_ss(tmem + C::COL_S + 128 * b, sdesc_sw128(aq + oa, 16, 1024),
+                 sdesc_sw128(ring + sl[h] * C::ITEM + ob, 16, 1024), kIdS, kk > 0);
         }
         mma_commit(&s_full[b]);
-        mma_commit(&ring_empty[slot]);
+        for (int h = 0; h < C::PER; ++h) mma_commit(&ring_empty[sl[h]]);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, status, kStatusTimeout);
-      int slot;
-      if (ok && (ok = take(slot))) {
-        tc_fence_after();
-        issue_s(0, slot);
-      }
-      if (ok && n > 1 && (ok = take(slot))) {
-        tc_fence_after();
-        issue_s(1, slot);
-      }
+      int sl[C::PER];
+      if (ok && (ok = take_tile(sl))) issue_s(0, sl);
+      if (ok && n > 1 && (ok = take_tile(sl))) issue_s(1, sl);
       for (int j = 0; ok && j < n; ++j) {
         const int b = j & 1;
         if (!(ok = mbar_wait(&p_full[b], (j >> 1) & 1, abort_flag, status, kStatusTimeout))) break;
-        if (!(ok = take(slot))) break;  // V_j
-        tc_fence_after();
-        const uint64_t dv = sdesc_sw128(ring + slot * C::TILE, C::SLAB, 1024);
+        if (!(ok = take_tile(sl))) break;  // V_j
+        for (int h = 0; h < C::PER; ++h) {  // O (or its feature half h) += P V_j
+          const uint64_t dv = sdesc_sw128(ring + sl[h] * C::ITEM, C::SLAB, 1024);
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + C::COL_O, tmem + C::COL_S + 128 * b + 8 * kk, dv + ((kk * 2048) >> 4), kIdPV,
-                 j > 0 || kk > 0);
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ts(tmem + C::COL_O + (D / C::PER) * h, tmem + C::COL_S + 128 * b + 8 * kk,
+                   dv + ((kk * 2048) >> 4), kIdPV, j > 0 || kk > 0);
+        }
         mma_commit(&pv_done[b]);
-        mma_commit(&ring_empty[slot]);
+        for (int h = 0; h < C::PER; ++h) mma_commit(&ring_empty[sl[h]]);
         // S(j+2) overwrites P(j): after PV(j), from the same thread (in order)
         if (j + 2 < n) {
-          if (!(ok = take(slot))) break;  // K_(j+2)
-          tc_fence_after();
-          issue_s(b, slot);
+          if (!(ok = take_tile(sl))) break;  // K_(j+2)
+          issue_s(b, sl);
         }
       }
       if (ok) {
@@ -376,6 +389,10 @@ cudaError_t launch_decode_tc(int d, bool bf16, const DecodeArgs& a, cudaStream_t
   FA_DEC_CASE(128, false, true)
   FA_DEC_CASE(128, true, false)
   FA_DEC_CASE(128, true, true)
+  FA_DEC_CASE(256, false, false)
+  FA_DEC_CASE(256, false, true)
+  FA_DEC_CASE(256, true, false)
+  FA_DEC_CASE(256, true, true)
 #undef FA_DEC_CASE
   return cudaErrorInvalidValue;
 }

@@ -142,9 +142,6 @@ cudaError_t launch_backward_dq_convert(int d, bool bf16, const float* dq_accum, 
 cudaError_t launch_selftest_wait_timeout(unsigned int* status, cudaStream_t stream);
 
 struct DecodeArgs {
-  const void* q;       // [B*H, Nq, d]
-  const void* k;       // [B*H, Nk, d]
-  const void* v;       // [B*H, Nk, d]
   void* o;             // [B*H, Nq, d]
   float* lse;          // [B*H, Nq]
   float* o_part;       // [num_splits, B*H, Nq, d] float32
@@ -154,19 +151,16 @@ struct DecodeArgs {
   int chunk;           // keys per split (multiple of 256)
   bool causal;
   float scale_log2;
-  // the tensor-core kernel (decode_uses_tc): 3-D maps over q, k, v, box 64 columns x 128 rows
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over q, k, v, box 64 columns x 128 rows
   unsigned int* status = nullptr;
 };
-// Decoding at d <= 128 runs on the tensor cores (fa_decode_tc.cu): streaming K
-// and V, it reached 84-90% of the HBM bandwidth at 1 to 128 queries per head,
-// against 80% (one query) down to 16% (sixteen) for the CUDA-core kernel,
-// which keeps d = 256.
-inline bool decode_uses_tc(int Nq, int d) { return Nq >= 1 && d <= 128; }
+// Decoding runs on the tensor cores (fa_decode_tc.cu) at every head dimension:
+// streaming K and V it reached 85-91% of the HBM bandwidth from 1 to 64 queries
+// per head at d = 128 and d = 256, where a CUDA-core kernel (dot products of
+// up to 16 queries per key row on the FMA pipe) reached 78-80% at one query,
+// 18% at 16 and 5% at 64.
 int decode_default_splits(int BH, int Nq, int Nk);
-int decode_tc_default_splits(int BH, int Nq, int Nk);
 int decode_chunk(int Nk, int num_splits);
-cudaError_t launch_decode(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_tc(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_combine(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream);
 
