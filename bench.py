@@ -875,7 +875,9 @@ def run_gpu(args, w, world, rank, local):
         from exact_io_aware_forward_gb300.synth import D1
         import dataclasses
         for key, dw in (("decode", D1), ("decode_nq16", dataclasses.replace(D1, Nq=16, name="D1 Nq=16")),
-                        ("decode_nq64", dataclasses.replace(D1, Nq=64, name="D1 Nq=64"))):
+                        ("decode_nq64", dataclasses.replace(D1, Nq=64, name="D1 Nq=64")),
+                        ("decode_d256_nq16", dataclasses.replace(D1, H=16, d=256, Nq=16,
+                                                                 name="D1 shape at d=256 H=16 Nq=16"))):
             dms, dbytes, _ = measure_decode(dev, dw, 10, 3)
             dgbs = dbytes / (dms * 1e-3) / 1e9
             result[key] = {"workload": dw.name, "ms": round(dms, 4), "GB_per_s": round(dgbs, 1),
