@@ -258,8 +258,11 @@ def run_decode(args, world, rank, local):
 
     import exact_io_aware_forward_gb300 as fa
     from exact_io_aware_forward_gb300.synth import D1 as w
-    if args.nq != w.Nq:
-        w = dataclasses.replace(w, Nq=args.nq, name=f"D1 decode causal Nq={args.nq} Nk={w.Nk} d={w.d} {w.dtype}")
+    if args.decode_d != w.d:  # the same keys at another head dimension (d = 256: half the heads)
+        w = dataclasses.replace(w, d=args.decode_d, H=w.H if args.decode_d <= 128 else w.H // 2)
+    if args.nq != w.Nq or args.decode_d != 128:
+        w = dataclasses.replace(w, Nq=args.nq,
+                                name=f"D1 decode causal Nq={args.nq} Nk={w.Nk} H={w.H} d={w.d} {w.dtype}")
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -967,6 +970,8 @@ def main():
                          "16 causal sequences")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing (rank 0, N=1)")
     ap.add_argument("--nq", type=int, default=1, help="--mode decode: queries per head (1: the D1 workload)")
+    ap.add_argument("--decode-d", type=int, default=128, choices=[64, 128, 256],
+                    help="--mode decode: head dimension (256 runs the D1 keys with H = 16)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
