@@ -9,6 +9,7 @@ from .api import (FAError, backward, fa_backward, fa_backward_dkdv, fa_backward_
                   fa_backward_dk_dv, fa_backward_dq, fa_backward_dk_dv_blocksparse,
                   fa_backward_dq_blocksparse,
                   fa_backward_noalloc, fa_decode_workspace_size, fa_forward_decode, forward_decode,
+                  fa_decode_gqa_workspace_size, fa_forward_decode_gqa,
                   fa_forward_blocksparse, fa_backward_blocksparse, fa_backward_dkdv_blocksparse,
                   fa_forward_dropout, fa_backward_dropout, fa_backward_dkdv_dropout, fa_dropout_keep_mask,
                   fa_backward_dk_dv_dropout, fa_backward_dq_dropout,

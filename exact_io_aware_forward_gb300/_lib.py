@@ -40,6 +40,8 @@ SIGNATURES = {
     "fa_backward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
     "fa_forward_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "fa_decode_gqa_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_forward_decode_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "fa_forward_dropout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32, _P]),
     "fa_backward_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _U64, _U32, _P,
                                  _S, _P]),

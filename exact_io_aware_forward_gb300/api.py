@@ -452,6 +452,27 @@ def fa_forward_decode(q, k, v, o, lse, workspace, causal=False, scale=None, num_
                                                         workspace.numel(), _stream(stream)))
 
 
+def fa_decode_gqa_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits=0) -> int:
+    return int(lib().fa_decode_gqa_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits))
+
+
+def fa_forward_decode_gqa(q, k, v, o, lse, workspace, causal=False, scale=None, num_splits=0, stream=None) -> None:
+    """Split-KV forward with grouped queries: q, o [B,Hq,Nq,d]; k, v [B,Hkv,Nk,d]
+    (Hq a multiple of Hkv; query head h reads K / V head h // (Hq // Hkv)); lse [B,Hq,Nq]."""
+    B, Hq, Nq, d = _shape(q)
+    dt = q.dtype
+    if k.dim() != 4 or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k must be [B, Hkv, Nk, d] with q's B and d")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    args = [_bhnd("q", q), _bhnd("k", k, None, dt), _bhnd("v", v, k.shape, dt), _bhnd("o", o, q.shape, dt),
+            _bhnd("lse", lse, (B, Hq, Nq), torch.float32)]
+    _check("fa_forward_decode_gqa", lib().fa_forward_decode_gqa(
+        *args, B, Hq, Hkv, Nq, Nk, d, _DTYPE_CODE[dt], int(bool(causal)), _scale(scale, d), int(num_splits),
+        workspace.data_ptr(), workspace.numel(), _stream(stream)))
+
+
 def fa_selftest_wait_timeout(stream=None) -> None:
     """Enqueue the failure-detection self-test (a bounded wait that never
     completes; ~2 s); the next fa_device_status() raises FA_ERR_TIMEOUT."""
@@ -491,14 +512,20 @@ def forward(q, k, v, causal=False, scale=None, stream=None, block_mask=None, dro
 
 
 def forward_decode(q, k, v, causal=False, scale=None, num_splits=0, stream=None, workspace=None):
-    """Return (O, LSE) for few queries q [B,H,Nq,d] against k, v [B,H,Nk,d]."""
+    """Return (O, LSE) for few queries q [B,Hq,Nq,d] against k, v [B,Hkv,Nk,d]
+    (Hkv = Hq, or grouped queries: Hq a multiple of Hkv)."""
     B, H, Nq, d = _shape(q)
+    grouped = k.dim() == 4 and k.shape[1] != H
     if workspace is None:
-        n = fa_decode_workspace_size(B, H, Nq, k.shape[2], d, num_splits)
+        n = (fa_decode_gqa_workspace_size(B, H, k.shape[1], Nq, k.shape[2], d, num_splits) if grouped
+             else fa_decode_workspace_size(B, H, Nq, k.shape[2], d, num_splits))
         workspace = torch.empty(max(n, 1), device=q.device, dtype=torch.uint8)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
-    fa_forward_decode(q, k, v, o, lse, workspace, causal, scale, num_splits, stream)
+    if grouped:
+        fa_forward_decode_gqa(q, k, v, o, lse, workspace, causal, scale, num_splits, stream)
+    else:
+        fa_forward_decode(q, k, v, o, lse, workspace, causal, scale, num_splits, stream)
     return o, lse
 
 

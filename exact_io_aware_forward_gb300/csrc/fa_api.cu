@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/fa_gb300.h"
+#include "fa_decode.h"
 #include "fa_internal.h"
 
 namespace {
@@ -653,6 +654,15 @@ fa_status fa_dropout_keep_mask(uint8_t* keep, int BH, int Nq, int Nk, float p_dr
 // ---------------------------------------------------------------- decoding
 namespace {
 
+// Query rows of one K / V head when Hq query heads share Hkv K / V heads.
+fa_status gqa_rows(int Hq, int Hkv, int Nq, int* rows) {
+  if (Hq < 1 || Hkv < 1 || Nq < 1 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  const long long r = (long long)(Hq / Hkv) * Nq;
+  if (r > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  *rows = (int)r;
+  return FA_OK;
+}
+
 fa_status decode_plan(int B, int H, int Nq, int Nk, int d, int num_splits, int* splits, int* chunk,
                       size_t* bytes) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
@@ -683,10 +693,29 @@ size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d, int num_spl
 fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                             int Nq, int Nk, int d, int dtype, int causal, float scale, int num_splits,
                             void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_forward_decode_gqa(q, k, v, o, lse, B, H, H, Nq, Nk, d, dtype, causal, scale, num_splits, workspace,
+                               workspace_bytes, stream);
+}
+
+size_t fa_decode_gqa_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits) {
+  int rows;
+  if (gqa_rows(Hq, Hkv, Nq, &rows) != FA_OK) return 0;
+  int s, c;
+  size_t bytes = 0;
+  return decode_plan(B, Hkv, rows, Nk, d, num_splits, &s, &c, &bytes) == FA_OK ? bytes : 0;
+}
+
+fa_status fa_forward_decode_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                int Hkv, int Nq, int Nk, int d, int dtype, int causal, float scale, int num_splits,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  // The Hq / Hkv query heads of a K / V head are consecutive in q, o and lse,
+  // so they form one block of rows = (Hq / Hkv) * Nq query rows of that head.
+  int rows;
+  fa_status st = gqa_rows(Hq, Hkv, Nq, &rows);
+  if (st != FA_OK) return st;
   int splits, chunk;
   size_t need;
-  fa_status st = decode_plan(B, H, Nq, Nk, d, num_splits, &splits, &chunk, &need);
-  if (st != FA_OK) return st;
+  if ((st = decode_plan(B, Hkv, rows, Nk, d, num_splits, &splits, &chunk, &need)) != FA_OK) return st;
   if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
@@ -697,25 +726,25 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o
   fa::DecodeArgs a;
   a.o = o;
   a.lse = lse;
-  a.BH = B * H;
-  a.Nq = Nq;
+  a.BH = B * Hkv;
+  a.Nq = rows;
   a.Nk = Nk;
   a.num_splits = splits;
   a.chunk = chunk;
   a.causal = causal != 0;
   a.scale_log2 = scale * kLog2e;
-  const size_t rows = (size_t)splits * a.BH * Nq;
+  const size_t part_rows = (size_t)splits * a.BH * rows;
   a.o_part = static_cast<float*>(workspace);
-  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)));
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(part_rows * d * sizeof(float)));
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  Shape sh;
-  if (dense_shape(B, H, Nq, Nk, d, dtype, &sh) != FA_OK) return FA_ERR_INVALID_ARG;
+  Shape sh;  // q viewed as [B, Hkv, rows, d], k and v as [B, Hkv, Nk, d]
+  if (dense_shape(B, Hkv, rows, Nk, d, dtype, &sh) != FA_OK) return FA_ERR_INVALID_ARG;
   if (!make_map(&a.tm_q, q, sh, false, 128) || !make_map(&a.tm_k, k, sh, true, 128) ||
       !make_map(&a.tm_v, v, sh, true, 128))
     return FA_ERR_CUDA;
   a.status = status_word();
   if (!a.status) return FA_ERR_CUDA;
-  if (fa::launch_decode_tc(d, dtype == FA_BF16, a, cs) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::launch_decode_tc_grouped(d, dtype == FA_BF16, a, Nq, cs) != cudaSuccess) return FA_ERR_CUDA;
   return fa::launch_decode_combine(d, dtype == FA_BF16, a, cs) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

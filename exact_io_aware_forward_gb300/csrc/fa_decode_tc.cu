@@ -24,6 +24,11 @@
 // Causal (queries are the last Nq of Nk positions): key j is visible to
 // query i iff j <= i + Nk - Nq; tiles past the query tile's last visible key
 // are not read, a chunk no query of the tile sees writes LSE_s = -inf.
+// Grouped queries (several query heads per K / V head): the query heads of
+// one K / V head are consecutive in memory, so their rows form one longer
+// query block of that head; row R of it is query R % qph (qph queries per
+// head) of query head R / qph, and only the causal position uses qph.
+#include "fa_decode.h"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -79,16 +84,21 @@ template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(256, 1)
     fa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o_part,
-                        float* __restrict__ lse_part, int Nq, int Nk, int BH, int chunk, float scale_log2,
-                        unsigned int* status) {
+                        float* __restrict__ lse_part, int Nq, int qph, int Nk, int BH, int chunk,
+                        float scale_log2, unsigned int* status) {
   using C = DecTcCfg<D>;
   const int split = blockIdx.x, bh = blockIdx.y;
-  const int q0 = blockIdx.z * C::BM;
+  const int q0 = blockIdx.z * C::BM;        // rows of this K / V head: Nq = query heads x qph
   const int nq = min(C::BM, Nq - q0);
-  const int off = Nk - Nq;  // causal: key visible iff key <= query + off
+  const int off = Nk - qph;  // causal: key visible iff key <= position + off
+  // query positions of the tile's rows (row R at position R % qph)
+  const int p0 = q0 % qph;
+  const bool wraps = p0 + nq > qph;  // the tile spans two query heads
+  const int pmin = wraps ? 0 : p0;
+  const int pmax = wraps ? qph - 1 : p0 + nq - 1;
   const int kb = split * chunk;
   int ke = min(Nk, kb + chunk);
-  if (CAUSAL) ke = min(ke, q0 + nq + off);  // one past the last key the tile's last query sees
+  if (CAUSAL) ke = min(ke, pmax + 1 + off);  // one past the last key the tile's rows see
   const int n = ke > kb ? (ke - kb + C::BN - 1) / C::BN : 0;
   const long long part_row = (long long)split * BH * Nq + (long long)bh * Nq + q0;
   if (n == 0) {  // no query of this tile sees a key of the chunk: weight 0 in the combine
@@ -238,8 +248,7 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ softmax, epilogue
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const int q = q0 + r;            // this thread's query
-    const int q_off = q + off;       // causal: key visible iff key <= q_off
+    const int q_off = (q0 + r) % qph + off;  // causal: this row's key visible iff key <= q_off
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_ref = neg_inf(), l = 0.f, l_mma = 0.f;
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(s[cc]);
       const int kbase = kb + j * C::BN;
-      const bool need_mask = (kbase + C::BN > ke) || (CAUSAL && kbase + C::BN - 1 > q0 + off);
+      const bool need_mask = (kbase + C::BN > ke) || (CAUSAL && kbase + C::BN - 1 > pmin + off);
       if (need_mask) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -365,22 +374,23 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 template <int D, bool CAUSAL, bool BF16>
-cudaError_t launch_dec_tc_t(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_dec_tc_t(const DecodeArgs& a, int qph, cudaStream_t stream) {
   using C = DecTcCfg<D>;
   auto kern = fa_decode_tc_kernel<D, CAUSAL, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_splits, a.BH, (a.Nq + C::BM - 1) / C::BM);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o_part, a.lse_part, a.Nq, a.Nk, a.BH,
-                                               a.chunk, a.scale_log2, a.status);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o_part, a.lse_part, a.Nq, qph, a.Nk,
+                                               a.BH, a.chunk, a.scale_log2, a.status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode_tc(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode_tc_grouped(int d, bool bf16, const DecodeArgs& a, int q_per_head, cudaStream_t stream) {
+  if (q_per_head < 1 || a.Nq % q_per_head != 0) return cudaErrorInvalidValue;
 #define FA_DEC_CASE(DD, CC, BB) \
-  if (d == DD && a.causal == CC && bf16 == BB) return launch_dec_tc_t<DD, CC, BB>(a, stream);
+  if (d == DD && a.causal == CC && bf16 == BB) return launch_dec_tc_t<DD, CC, BB>(a, q_per_head, stream);
   FA_DEC_CASE(64, false, false)
   FA_DEC_CASE(64, false, true)
   FA_DEC_CASE(64, true, false)
@@ -395,6 +405,10 @@ cudaError_t launch_decode_tc(int d, bool bf16, const DecodeArgs& a, cudaStream_t
   FA_DEC_CASE(256, true, true)
 #undef FA_DEC_CASE
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_tc(int d, bool bf16, const DecodeArgs& a, cudaStream_t stream) {
+  return launch_decode_tc_grouped(d, bf16, a, a.Nq, stream);
 }
 
 }  // namespace fa

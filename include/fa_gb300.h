@@ -366,6 +366,23 @@ fa_status fa_forward_decode(const void* q, const void* k, const void* v, void* o
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Split-KV decoding with grouped queries: Hq query heads share Hkv K / V heads
+ * (Hq a multiple of Hkv; query head h reads K / V head h / (Hq / Hkv)).
+ * q, o: [B,Hq,Nq,d]; k, v: [B,Hkv,Nk,d]; lse: [B,Hq,Nq] float32.  Every query
+ * head gets what fa_forward_decode gives it against its K / V head (causal:
+ * query i of every head at position i + Nk - Nq), but each K / V chunk is read
+ * once for all the query heads that share it.  workspace:
+ * fa_decode_gqa_workspace_size(B,Hq,Hkv,Nq,Nk,d,num_splits) bytes (0 for
+ * invalid sizes).  Hq not a multiple of Hkv, or Hq, Hkv < 1, gives
+ * FA_ERR_INVALID_ARG; other arguments and errors as fa_forward_decode (which
+ * is this call with Hq = Hkv = H).
+ */
+size_t fa_decode_gqa_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits);
+fa_status fa_forward_decode_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                int Hkv, int Nq, int Nk, int d, int dtype, int causal, float scale, int num_splits,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Size of the fixed device scratch array used by fa_backward_noalloc.
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

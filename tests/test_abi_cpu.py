@@ -178,3 +178,20 @@ def test_head_dim_256_has_no_block_mask(lib):
     rc = lib.fa_backward_blocksparse(ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 1, 1, 64, 256, 1, 0,
                                      0.0625, ptr, 1 << 30, None)
     assert rc == 2
+
+
+def test_grouped_query_decode_validation(lib):
+    """Query heads not a multiple of the K / V heads are rejected before any
+    launch; the workspace of grouped decoding is that of plain decoding over
+    the K / V heads with their query heads' rows stacked."""
+    ptr = 1 << 20
+    assert lib.fa_decode_gqa_workspace_size(1, 8, 3, 1, 1000, 128, 0) == 0
+    assert lib.fa_decode_gqa_workspace_size(1, 8, 0, 1, 1000, 128, 0) == 0
+    for splits in (0, 5):
+        assert lib.fa_decode_gqa_workspace_size(2, 8, 2, 3, 1000, 128, splits) == \
+            lib.fa_decode_workspace_size(2, 2, 12, 1000, 128, splits)
+    assert lib.fa_decode_gqa_workspace_size(1, 4, 4, 2, 300, 64, 0) == lib.fa_decode_workspace_size(1, 4, 2, 300, 64, 0)
+    rc = lib.fa_forward_decode_gqa(ptr, ptr, ptr, ptr, ptr, 1, 8, 3, 1, 1000, 128, 1, 1, 0.125, 0, ptr, 1 << 30, None)
+    assert rc == 1
+    rc = lib.fa_forward_decode_gqa(ptr, ptr, ptr, ptr, ptr, 1, 8, 2, 10, 5, 128, 1, 1, 0.125, 0, ptr, 1 << 30, None)
+    assert rc == 1  # causal with more queries than keys

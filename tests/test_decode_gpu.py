@@ -42,7 +42,7 @@ CASES = [
     (1, 2, 3, 1000, 64, "bf16", True, 7), (1, 2, 4, 1000, 128, "fp16", False, 3), (2, 2, 5, 4100, 128, "bf16", True, 0),
     (1, 3, 16, 700, 64, "fp16", True, 1), (1, 2, 17, 2000, 128, "bf16", True, 9), (1, 1, 40, 40, 128, "bf16", True, 0),
     (2, 2, 40, 5000, 64, "bf16", False, 0), (1, 2, 8, 257, 128, "fp16", True, 64),
-    # 8 queries or more at d <= 128: the tensor-core split kernel (128-query tiles)
+    # several query tiles of 128 rows
     (1, 2, 64, 3333, 128, "bf16", True, 0), (1, 2, 128, 1000, 64, "fp16", False, 0),
     (1, 1, 129, 4097, 128, "bf16", True, 0), (2, 1, 200, 1500, 128, "fp16", True, 3),
     (1, 2, 9, 130, 64, "bf16", False, 0), (1, 2, 100, 100, 128, "bf16", True, 1),
@@ -99,3 +99,52 @@ def test_decode_full_size_several_queries(nq):
     fa.fa_device_status()
     eo, el = _check(q, k, v, o.cpu(), lse.cpu(), True, heads=[(0, 0), (2, 9), (3, 31)])
     assert eo <= O_TOL["bf16"] and el <= LSE_TOL, (eo, el)
+
+
+GQA_CASES = [  # B, Hq, Hkv, Nq, Nk, d, dtype, causal, splits
+    (1, 8, 2, 1, 3000, 128, "bf16", True, 0), (2, 8, 1, 3, 1000, 64, "fp16", True, 7),
+    (1, 16, 4, 16, 2000, 128, "bf16", True, 0), (1, 12, 3, 40, 700, 256, "bf16", True, 0),
+    (1, 4, 2, 100, 100, 128, "fp16", False, 3), (1, 6, 6, 5, 500, 64, "bf16", True, 0),
+    (2, 32, 4, 1, 4097, 256, "fp16", True, 0),
+]
+
+
+def _gqa_inputs(B, Hq, Hkv, Nq, Nk, d, dtype, seed):
+    q, _, _, _ = attention_inputs(B, Hq, Nq, d, dtype, seed=seed, with_do=False)
+    _, k, v, _ = attention_inputs(B, Hkv, Nk, d, dtype, seed=seed + 1, with_do=False)
+    return q, k, v
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,dtype,causal,splits", GQA_CASES)
+def test_grouped_query_decode_matches_oracle(B, Hq, Hkv, Nq, Nk, d, dtype, causal, splits):
+    """Query head h against K / V head h // (Hq // Hkv): each head as its own
+    rectangular problem in the oracle (tiles of 128 rows span several query
+    heads on the GPU; the causal position of a row is its query index)."""
+    q, k, v = _gqa_inputs(B, Hq, Hkv, Nq, Nk, d, dtype, seed=31 * Hq + Nq)
+    dev = torch.device("cuda:0")
+    o, lse = fa.forward_decode(q.to(dev), k.to(dev), v.to(dev), causal=causal, num_splits=splits)
+    fa.fa_device_status()
+    g = Hq // Hkv
+    s = 1.0 / math.sqrt(d)
+    qf, kf, vf = as_float64(q, k, v)
+    of, lf = o.cpu().double().numpy(), lse.cpu().double().numpy()
+    eo = el = 0.0
+    for b in range(B):
+        for h in range(Hq):
+            ro, rl = A.forward_head(qf[b, h], kf[b, h // g], vf[b, h // g], s, causal)
+            eo = max(eo, float(np.abs(of[b, h] - ro).max()))
+            el = max(el, float(np.abs(lf[b, h] - rl).max()))
+    assert eo <= O_TOL[dtype] and el <= LSE_TOL, (eo, el)
+
+
+def test_grouped_query_decode_equals_repeated_heads():
+    """With the same key chunks, grouped queries give bit for bit what plain
+    decoding gives with every K / V head repeated for its query heads."""
+    B, Hq, Hkv, Nq, Nk, d = 2, 8, 2, 7, 2500, 128
+    dev = torch.device("cuda:0")
+    q, k, v = (x.to(dev) for x in _gqa_inputs(B, Hq, Hkv, Nq, Nk, d, "bf16", seed=77))
+    o1, l1 = fa.forward_decode(q, k, v, causal=True, num_splits=3)
+    kr, vr = (x.repeat_interleave(Hq // Hkv, dim=1).contiguous() for x in (k, v))
+    o2, l2 = fa.forward_decode(q, kr, vr, causal=True, num_splits=3)
+    fa.fa_device_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
