@@ -165,3 +165,33 @@ def test_head_dim_workloads_full_size(name):
             ref = A.backward_head_rows(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, w.causal, r)
             assert rel_fro(dq[b, h].double().numpy()[r], ref) <= GRAD_REL_FRO, (b, h)
     _invariants(dk, dv, do)
+
+
+def test_noncausal_c4_shape_full_size():
+    """The C4 shape without the causal mask (non-causal d = 128 runs the one-shot
+    forward and the split backward over every key tile): two whole heads of
+    gradients, O / LSE and dQ rows of every head, the sum invariants."""
+    import dataclasses
+    w = dataclasses.replace(WORKLOADS["C4"], causal=False)
+    q, k, v, do = workload_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, causal=False)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=False)
+    fa.fa_device_status()
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    qf, kf, vf, dof = as_float64(q, k, v, do)
+    s = 1.0 / math.sqrt(w.d)
+    rng = np.random.default_rng(14)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        want = A.backward_head(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, False)
+        _check_head_grads([x[b, h].double().numpy() for x in (dq, dk, dv)], want)
+    for b in range(w.B):
+        for h in range(w.H):
+            r = _rows(w.N, rng, 4)
+            ro, rl = A.forward_head(qf[b, h], kf[b, h], vf[b, h], s, False, rows=r)
+            assert float(np.abs(o[b, h].double().numpy()[r] - ro).max()) <= O_TOL[w.dtype], (b, h)
+            assert float(np.abs(lse[b, h].double().numpy()[r] - rl).max()) <= LSE_TOL, (b, h)
+            ref = A.backward_head_rows(qf[b, h], kf[b, h], vf[b, h], dof[b, h], s, False, r)
+            assert rel_fro(dq[b, h].double().numpy()[r], ref) <= GRAD_REL_FRO, (b, h)
+    _invariants(dk, dv, do)
